@@ -1,0 +1,54 @@
+"""Pin strength: plausible mistakes planted in copies of the oracle must fail a pin.
+
+Each case edits one line of oracle.c in a temporary copy (on the CPU), builds
+it, and runs tests/test_oracle.py against that library in a child process.
+The pins must reject every mutant.
+"""
+from __future__ import annotations
+
+import os
+import shutil
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SRC = os.path.join(ROOT, "oracle", "oracle.c")
+
+MUTANTS = {
+    # Swapping the nibble order of BOTH operands permutes k inside one scale block
+    # on both sides and leaves D unchanged, so only a one-sided swap is a bug.
+    "nibble_order_swapped_in_a": ("oracle_e2m1(nibble(a_row, k))", "oracle_e2m1(nibble(a_row, k ^ 1))"),
+    "scale_block_fixed_16": ("scale_value(sa_row[k / vec], vec)", "scale_value(sa_row[k / 16], vec)"),
+    "b_scaled_by_a_scale": ("scale_value(sb_row[k / vec], vec)", "scale_value(sa_row[k / vec], vec)"),
+    "e2m1_subnormal_wrong": ("0.5 * (double)m : ldexp", "1.0 * (double)m : ldexp"),
+    "e4m3_bias_off": ("ldexp(1.0 + (double)m / 8.0, (int)e - 7)", "ldexp(1.0 + (double)m / 8.0, (int)e - 6)"),
+    "e8m0_bias_off": ("ldexp(1.0, (int)code - 127)", "ldexp(1.0, (int)code - 128)"),
+    "alpha_dropped": ("return alpha * sum;", "return sum;"),
+    "b_row_transposed": ("*b_row = B + j * row_bytes", "*b_row = B + (j % (i + 1)) * row_bytes"),
+    "sign_of_a_dropped": ("double a = oracle_e2m1(nibble(a_row, k))", "double a = oracle_e2m1(nibble(a_row, k) & 7u)"),
+    "bf16_ties_away": ("double q = nearbyint(ldexp(a, -q_exp));", "double q = round(ldexp(a, -q_exp));"),
+    "bf16_no_subnormal_floor": ("if (q_exp < -133) q_exp = -133;", "if (q_exp < -140) q_exp = -140;"),
+    "reorder_column_reversed": ("+ (c % 4);", "+ (3 - c % 4);"),
+    "reorder_rows_blocked_not_strided": ("off = (r % 32) * 16 + ((r / 32) % 4) * 4",
+                                         "off = ((r % 128) / 4) * 16 + (r % 4) * 4"),
+    "reorder_atoms_row_major_by_k": ("(r / 128) * kc4 + c / 4", "(c / 4) * ((rows + 127) / 128) + r / 128"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_reject_mutant(name, tmp_path):
+    old, new = MUTANTS[name]
+    src = open(SRC).read()
+    assert src.count(old) == 1, "mutation site not found: %s" % name
+    mutated = tmp_path / "oracle.c"
+    mutated.write_text(src.replace(old, new))
+    lib = tmp_path / "mutant.so"
+    subprocess.run(["gcc", "-O1", "-std=c11", "-fopenmp", "-ffp-contract=off", "-shared", "-fPIC",
+                    str(mutated), "-o", str(lib), "-lm"], check=True)
+    env = dict(os.environ, FP4_ORACLE_LIB=str(lib))
+    r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-p", "no:cacheprovider",
+                        os.path.join(ROOT, "tests", "test_oracle.py")],
+                       cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
+    assert r.returncode != 0, "mutant %s survived the pins:\n%s" % (name, r.stdout[-2000:])
