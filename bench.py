@@ -1,0 +1,352 @@
+"""Benchmark of the block-scaled FP4 GEMM on GB300 (one JSON line on stdout).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--results PATH]
+
+A step is one pass of the whole hot path over one problem: the scale reorder
+of sfA and sfB into the 128x4 atom layout, then the persistent tcgen05 GEMM on
+the reordered scales -- exactly what fp4_gemm_nvfp4 / fp4_gemm_mxfp4 launch --
+each a C-ABI call. Inputs are seeded synthetic data resident in HBM; L2 is
+flushed (a 256 MiB write) between timed steps, outside each step's events.
+
+`value` is whole-job TFLOP/s (2*M*N*K per step, summed over ranks, divided by
+the slowest rank's time). `roofline` is for the GEMM kernel: its FLOPs per
+launch over its CUDA-event duration, against the dense FP4 tensor peak (the
+measured bf16 burst peak times the nominal FP4:bf16 ratio 13.5:2.25 = 6).
+`e2e` is the same metric through fp4_gemm_host with pinned host buffers, the
+host<->device copies inside the timed region. `cpu_baseline` is the fp64 CPU
+oracle on a bounded row sample of the same problem, on all host cores.
+
+Multi-GPU (torchrun): replicas only -- every rank runs the same problem on its
+own GPU with no collective in the data path (weak scaling).
+
+--impl reference times the CPU oracle (the only reference this project has)
+on the same workload, one bounded row sample per step.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+METRIC = "block-scaled FP4 GEMM TFLOP/s on 1 GB300 and % of dense FP4 tensor peak"
+DEFAULT_WORKLOAD = "nvfp4_4096_bf16"
+FP4_PER_BF16 = 13.5 / 2.25       # nominal dense FP4 : dense bf16 tensor throughput on GB300
+FALLBACK_BF16_TFLOPS = 1900.0
+FALLBACK_HBM_GBS = 6800.0
+L2_FLUSH_BYTES = 256 << 20
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["bf16_tflops"]), float(p["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_BF16_TFLOPS, FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for rel in ("block_scaled_fp4_sfa_gb300/csrc/fp4_gemm.cu", "block_scaled_fp4_sfa_gb300/csrc/ptx.cuh"):
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(workload):
+    """DRAM bytes per GEMM launch from the committed ncu summary, if it was taken
+    on the current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", "gemm_traffic.json")
+    try:
+        with open(path) as f:
+            t = json.load(f)
+    except (OSError, ValueError):
+        return None
+    e = t.get(workload)
+    if not e or e.get("kernel_hash") != kernel_source_hash():
+        return None
+    return float(e["dram_bytes_per_launch"])
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling while the timed region runs."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.Q,
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in getattr(self, "lines", []):
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def oracle_rows_tflops(inp, rows, nthreads=0):
+    import oracle
+    t0 = time.perf_counter()
+    oracle.gemm_rows(inp, rows, nthreads=nthreads)
+    dt = time.perf_counter() - t0
+    return 2.0 * len(rows) * inp.N * inp.K / dt / 1e12, dt
+
+
+def cpu_sample_rows(inp, target_s):
+    """Row sample whose oracle time is about target_s seconds (at least 1 row)."""
+    probe = np.arange(min(2, inp.M))
+    _, dt = oracle_rows_tflops(inp, probe)
+    per_row = dt / len(probe)
+    n = int(max(1, min(inp.M, target_s / max(per_row, 1e-9))))
+    return np.linspace(0, inp.M - 1, n).astype(np.int64)
+
+
+def run_reference(args, inp):
+    """The CPU oracle timed as the reference arm: each step one bounded row sample."""
+    rows = cpu_sample_rows(inp, args.ref_step_s)
+    for _ in range(args.warmup):
+        oracle_rows_tflops(inp, rows[: max(1, len(rows) // 8)])
+    times = []
+    for _ in range(args.steps):
+        _, dt = oracle_rows_tflops(inp, rows)
+        times.append(dt)
+    flops = 2.0 * len(rows) * inp.N * inp.K
+    value = flops * len(times) / sum(times) / 1e12
+    cores = os.cpu_count()
+    sample = "%d of %d rows of %s (all %d columns), fp64 C oracle, OpenMP" % (len(rows), inp.M, inp.name, inp.N,
+                                                                            cores)
+    return {"metric": METRIC, "value": value, "unit": "TFLOP/s", "impl": "reference", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sum(times) / len(times),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": workload_config(inp),
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def workload_config(inp):
+    return {"workload": inp.name, "format": inp.fmt, "M": inp.M, "N": inp.N, "K": inp.K, "out": inp.out,
+            "alpha": inp.alpha, "l2": "flushed between steps (256 MiB write, outside the step events)"}
+
+
+def run_ours(args, inp, rank, ws, local):
+    import torch
+    import block_scaled_fp4_sfa_gb300 as fp4
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    fp4.load()
+    stream = torch.cuda.current_stream()
+    vec = inp.vec
+    hA, hsA, hB, hsB = (torch.from_numpy(np.ascontiguousarray(getattr(inp, k))) for k in ("A", "sfA", "B", "sfB"))
+    A, sfA, B, sfB = (t.to(dev) for t in (hA, hsA, hB, hsB))
+    atomA = torch.empty(fp4.scale_atom_bytes(inp.M, inp.K, vec), dtype=torch.uint8, device=dev)
+    atomB = torch.empty(fp4.scale_atom_bytes(inp.N, inp.K, vec), dtype=torch.uint8, device=dev)
+    odt = torch.float32 if inp.out == "f32" else torch.bfloat16
+    D = torch.empty(inp.M, inp.N, dtype=odt, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    prepacked = fp4.gemm_nvfp4_prepacked if inp.fmt == "nvfp4" else fp4.gemm_mxfp4_prepacked
+    s = stream.cuda_stream
+
+    def step():
+        fp4.scale_reorder(sfA, atomA, inp.M, inp.K, vec, stream=s)
+        fp4.scale_reorder(sfB, atomB, inp.N, inp.K, vec, stream=s)
+        ev_g0.record(stream)
+        prepacked(A, atomA, B, atomB, inp.alpha, D, inp.M, inp.N, inp.K, inp.out, stream=s)
+        ev_g1.record(stream)
+
+    ev_g0 = torch.cuda.Event(enable_timing=True)
+    ev_g1 = torch.cuda.Event(enable_timing=True)
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    st = fp4.get_device_status(s)
+    if st != 0:
+        raise RuntimeError("device status after warm-up: %s" % fp4.status_string(st))
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    g0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    g1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        time.sleep(0.2)
+        t_wall0 = time.perf_counter()
+        for i in range(args.steps):
+            flush.zero_()
+            starts[i].record(stream)
+            ev_g0, ev_g1 = g0[i], g1[i]
+            step()
+            ends[i].record(stream)
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter() - t_wall0
+        if ws > 1:
+            torch.distributed.barrier()
+    st = fp4.get_device_status(s)
+    if st != 0:
+        raise RuntimeError("device status after timing: %s" % fp4.status_string(st))
+    step_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+    gemm_ms = [a.elapsed_time(b) for a, b in zip(g0, g1)]
+    total_ms = sum(step_ms)
+    if ws > 1:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = inp.flops * args.steps * ws / (total_ms * 1e-3) / 1e12
+
+    # e2e: host buffers through fp4_gemm_host, pinned memory, copies inside the timed region
+    pA, psA, pB, psB = (t.pin_memory() for t in (hA, hsA, hB, hsB))
+    pD = torch.empty(inp.M, inp.N, dtype=odt).pin_memory()
+    e_steps = max(3, min(args.steps, 20))
+    for _ in range(2):
+        fp4.gemm_host(inp.fmt, pA, psA, pB, psB, inp.alpha, pD, inp.M, inp.N, inp.K, inp.out, stream=s)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e_steps):
+        fp4.gemm_host(inp.fmt, pA, psA, pB, psB, inp.alpha, pD, inp.M, inp.N, inp.K, inp.out, stream=s)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e_steps
+    h2d = sum(t.numel() * t.element_size() for t in (hA, hsA, hB, hsB))
+    d2h = pD.numel() * pD.element_size()
+
+    bf16_peak, hbm_peak, peak_src = peaks()
+    gemm_avg_ms = sum(gemm_ms) / len(gemm_ms)
+    achieved = inp.flops / (gemm_avg_ms * 1e-3) / 1e12
+    fp4_peak = bf16_peak * FP4_PER_BF16
+    traffic = ncu_traffic(inp.name)
+    alg_bytes = (inp.M + inp.N) * (inp.K // 2 + inp.K // vec) + inp.M * inp.N * (4 if inp.out == "f32" else 2)
+    result = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "e2m1", "data": "synthetic",
+        "config": dict(workload_config(inp), parallelism="replicas" if ws > 1 else "single"),
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": fp4_peak, "unit": "TFLOP/s",
+                     "frac": achieved / fp4_peak, "traffic": traffic,
+                     "peak_source": "%s bf16 burst %.1f TFLOP/s x %.0f (nominal FP4:bf16)" % (peak_src, bf16_peak,
+                                                                                            FP4_PER_BF16),
+                     "kernel": "fp4_gemm_kernel", "gemm_us": 1e3 * gemm_avg_ms,
+                     "algorithmic_bytes": alg_bytes,
+                     "hbm_frac_at_algorithmic_bytes": alg_bytes / (gemm_avg_ms * 1e-3) / 1e9 / hbm_peak},
+        "e2e": {"value": inp.flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": 3 * args.steps,
+        "clocks": clk.summary(),
+        "wall_s_timed_region": t_wall,
+    }
+    return result
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=W.config_names())
+    ap.add_argument("--cpu-sample-s", type=float, default=12.0, help="oracle seconds for cpu_baseline")
+    ap.add_argument("--ref-step-s", type=float, default=3.0, help="oracle seconds per reference step")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--results", default=None, help="also append the JSON line to this file")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    ws, rank, local = dist_env()
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        inp = W.make_config(args.workload)
+        res = run_reference(args, inp)
+    else:
+        if ws > 1:
+            import torch
+            torch.cuda.set_device(local)
+            torch.distributed.init_process_group("nccl")
+        inp = W.make_config(args.workload)
+        res = run_ours(args, inp, rank, ws, local)
+        if rank == 0 and not args.no_cpu_baseline:
+            rows = cpu_sample_rows(inp, args.cpu_sample_s)
+            v, dt = oracle_rows_tflops(inp, rows)
+            res["cpu_baseline"] = {"value": v, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
+                                   "sample": "%d of %d rows of %s (all %d columns), %.1f s, fp64 C oracle"
+                                             % (len(rows), inp.M, inp.name, inp.N, dt)}
+        if ws > 1:
+            import torch
+            torch.distributed.destroy_process_group()
+    if rank == 0:
+        line = json.dumps(res)
+        print(line, flush=True)
+        if args.results:
+            with open(args.results, "a") as f:
+                f.write(line + "\n")
+
+
+if __name__ == "__main__":
+    main()

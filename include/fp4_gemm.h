@@ -1,0 +1,145 @@
+/*
+ * fp4_gemm.h -- C ABI of the GB300 (sm_103a) block-scaled FP4 GEMM.
+ *
+ *   D = alpha * ( decode(A, sfA) . decode(B, sfB)^T )
+ *
+ * The operation: a blockwise-scaled GEMM on E2M1 (Float4E2M1FN) operands,
+ * computed by the block-scaled FP4 MMA ("[BUG] Add FP4 TMA kernel example for
+ * Blackwell in CuTe Python DSL", CUTLASS issue #2922, sections "Summary",
+ * "Background" and "What Works": MmaMXF4NVF4Op). Two scale formats:
+ *   - NVFP4: one E4M3 scale per 16 K-elements (same issue, section "Scale
+ *     Factor Granularity": sf_vec_size = 16, Float8E4M3FN scales);
+ *   - MXFP4: one E8M0 scale per 32 K-elements ("TMA Pipelines, Tensor Cores,
+ *     and ctm-rs Interop", section 1, "Block-Scaled MXFP4 GEMM in cute-rs
+ *     (SM120a)": Float8E8M0FNU scales).
+ * The block-scaled MMA consumes K = 64 FP4 elements per instruction (issue
+ * #2922, section "MMA Instruction K Constraint").
+ *
+ * Layouts (all row-major, contiguous, on the device unless a call says host):
+ *   A    [M][K/2] bytes. Two E2M1 codes per byte, K-major: element k = 2j is
+ *        the low nibble of byte j, k = 2j + 1 the high nibble. ("Hopper GEMM
+ *        in CUTLASS C++ and the CuTe DSL, part 1", section on the swapped
+ *        operands, reason 3: both operands of the narrow GEMM are K-major.)
+ *   B    [N][K/2] bytes, same packing (the GEMM uses B transposed).
+ *   sfA  [M][K/vec] bytes, sfB [N][K/vec] bytes: plain row-major scale bytes
+ *        (E4M3 for NVFP4, vec = 16; E8M0 for MXFP4, vec = 32). E4M3 scales are
+ *        read as unsigned (sign bit must be 0); NaN scale bytes give
+ *        unspecified output.
+ *   "prepacked" scales: the same bytes in the 128x4 atom layout produced by
+ *        fp4_scale_reorder (rows padded to 128, scale columns to 4; atom
+ *        (rb, cb) at byte (rb * ceil(K/vec/4) + cb) * 512; row r, column c
+ *        inside it at (r % 32) * 16 + ((r / 32) % 4) * 4 + (c % 4); padding 0).
+ *   D    [M][N], fp32 or bf16 (round to nearest even), overwritten. No C, no beta.
+ *
+ * Requirements: K % 32 == 0; A, B, sfA, sfB, D 16-byte aligned. M, N, K >= 0;
+ * M == 0 or N == 0 is a no-op; K == 0 writes D = 0.
+ *
+ * Ownership: the caller owns every buffer; the library never frees them.
+ * Calls taking plain scales reorder them into stream-ordered scratch
+ * (cudaMallocAsync / cudaFreeAsync on `stream`); split-K partial sums use the
+ * same kind of scratch. Nothing else is allocated per call.
+ *
+ * Errors: argument problems return a status synchronously and launch nothing.
+ * Launch failures return FP4_ERR_CUDA. Every wait inside the kernels is
+ * bounded; a wait that runs out records FP4_ERR_TIMEOUT in a per-device status
+ * word that fp4_get_device_status reports. Calls are asynchronous with respect
+ * to the host and run on the current device.
+ */
+#ifndef FP4_GEMM_H
+#define FP4_GEMM_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    FP4_OK = 0,
+    FP4_ERR_INVALID_ARG = 1,   /* null pointer, negative size, unknown enum */
+    FP4_ERR_UNSUPPORTED = 2,   /* K % 32 != 0, size beyond the kernel's index range, bad config */
+    FP4_ERR_MISALIGNED = 3,    /* a pointer not 16-byte aligned */
+    FP4_ERR_CUDA = 4,          /* a CUDA runtime/driver call failed */
+    FP4_ERR_TIMEOUT = 5,       /* a bounded device wait ran out (reported by fp4_get_device_status) */
+    FP4_ERR_NO_DEVICE = 6      /* no device, or not an sm_103 device */
+} fp4_status;
+
+typedef enum { FP4_OUT_F32 = 0, FP4_OUT_BF16 = 1 } fp4_out_dtype;
+typedef enum { FP4_FMT_NVFP4 = 0, FP4_FMT_MXFP4 = 1 } fp4_format;
+
+/* Optional overrides of the launch plan (zero-initialise for "automatic").
+ *   mode:     0 auto; 1 direct (A on the 128-row MMA side, D written by TMA
+ *             store); 2 swap-AB (B on the 128-row side, D^T tiles written with
+ *             coalesced stores; the trick of "Hopper GEMM in CUTLASS C++ and
+ *             the CuTe DSL, part 1", section on the swapped operands).
+ *   bn:       0 auto; else the MMA N of a tile: 16, 32, 64, 128 or 256.
+ *             Several tiles along the N side need bn 128 or 256.
+ *   splits:   0 auto; else the number of K splits (swap-AB mode only).
+ *   max_ctas: 0 = one persistent CTA per SM; else a cap on the grid.         */
+typedef struct {
+    int32_t mode;
+    int32_t bn;
+    int32_t splits;
+    int32_t max_ctas;
+} fp4_gemm_config;
+
+/* NVFP4 GEMM (E4M3 scales, one per 16 K-elements), plain row-major scales. */
+fp4_status fp4_gemm_nvfp4(const void *A, const void *sfA, const void *B, const void *sfB,
+                          float alpha, void *D, int64_t M, int64_t N, int64_t K,
+                          fp4_out_dtype out, cudaStream_t stream);
+
+/* MXFP4 GEMM (E8M0 scales, one per 32 K-elements), plain row-major scales. */
+fp4_status fp4_gemm_mxfp4(const void *A, const void *sfA, const void *B, const void *sfB,
+                          float alpha, void *D, int64_t M, int64_t N, int64_t K,
+                          fp4_out_dtype out, cudaStream_t stream);
+
+/* Same GEMMs on scales already in the 128x4 atom layout (fp4_scale_reorder):
+ * the weight-side reorder can be done once and hoisted out of the hot loop. */
+fp4_status fp4_gemm_nvfp4_prepacked(const void *A, const void *sfA_atoms, const void *B,
+                                    const void *sfB_atoms, float alpha, void *D, int64_t M,
+                                    int64_t N, int64_t K, fp4_out_dtype out, cudaStream_t stream);
+fp4_status fp4_gemm_mxfp4_prepacked(const void *A, const void *sfA_atoms, const void *B,
+                                    const void *sfB_atoms, float alpha, void *D, int64_t M,
+                                    int64_t N, int64_t K, fp4_out_dtype out, cudaStream_t stream);
+
+/* General form of the four calls above, with an optional plan override (cfg may be NULL). */
+fp4_status fp4_gemm(fp4_format fmt, int scales_prepacked, const void *A, const void *sfA,
+                    const void *B, const void *sfB, float alpha, void *D, int64_t M, int64_t N,
+                    int64_t K, fp4_out_dtype out, const fp4_gemm_config *cfg, cudaStream_t stream);
+
+/* Host-buffer convenience form: A, sfA, B, sfB and D live in HOST memory
+ * (pinned for asynchronous copies). The call copies the inputs to stream-ordered
+ * device scratch, runs fp4_gemm, copies D back and returns; D is valid once
+ * `stream` has been synchronised. Same layouts and errors as fp4_gemm. */
+fp4_status fp4_gemm_host(fp4_format fmt, const void *A, const void *sfA, const void *B,
+                         const void *sfB, float alpha, void *D, int64_t M, int64_t N, int64_t K,
+                         fp4_out_dtype out, cudaStream_t stream);
+
+/* Bytes of the atom-layout copy of a rows x (k/vec) scale matrix (vec 16 or 32).
+ * Returns 0 for invalid arguments. */
+size_t fp4_scale_atom_bytes(int64_t rows, int64_t k, int vec);
+
+/* Scale reorder kernel: plain row-major sf[rows][k/vec] -> 128x4 atom layout
+ * (every byte of the fp4_scale_atom_bytes() output written, padding = 0).
+ * Both buffers on the device; sf_atom must not overlap sf_plain. */
+fp4_status fp4_scale_reorder(const void *sf_plain, void *sf_atom, int64_t rows, int64_t k,
+                             int vec, cudaStream_t stream);
+
+/* Synchronises `stream`, then returns and clears the current device's status
+ * word (FP4_OK, or FP4_ERR_TIMEOUT if a bounded wait ran out since the last call). */
+fp4_status fp4_get_device_status(cudaStream_t stream);
+
+/* Static description of a status code. */
+const char *fp4_status_string(fp4_status s);
+
+/* Bound on every device-side wait, in milliseconds (default 2000; also read once
+ * from the FP4_GEMM_WAIT_LIMIT_MS environment variable). Values < 1 are clamped to 1. */
+void fp4_set_wait_limit_ms(int64_t ms);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FP4_GEMM_H */

@@ -1,0 +1,112 @@
+"""The C-ABI library without a GPU: it builds, loads, exports every symbol that
+include/fp4_gemm.h declares, and rejects bad arguments on the host before any
+CUDA call. No compute call is made here."""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fp4_gemm.h")
+
+
+@pytest.fixture(scope="module")
+def fp4():
+    import block_scaled_fp4_sfa_gb300 as m
+    m.build()
+    return m
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fp4_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for must in ("fp4_gemm_nvfp4", "fp4_gemm_mxfp4", "fp4_gemm_nvfp4_prepacked", "fp4_gemm_mxfp4_prepacked",
+                 "fp4_scale_atom_bytes", "fp4_scale_reorder", "fp4_get_device_status", "fp4_status_string"):
+        assert must in names
+
+
+def test_library_exports_every_declared_symbol(fp4):
+    lib = fp4.load()
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_library_is_sm103a_only(fp4):
+    # the fatbin carries sm_103a SASS; the build flags name exactly one -gencode
+    from block_scaled_fp4_sfa_gb300 import _build
+    assert _build.ARCH == "-gencode=arch=compute_103a,code=sm_103a"
+    assert os.path.getsize(_build.LIB) > 0
+
+
+def test_status_strings(fp4):
+    for code in range(7):
+        assert fp4.status_string(code)
+    assert fp4.status_string(99) == "unknown status"
+
+
+@pytest.mark.parametrize("rows,K,vec", [(1, 32, 16), (128, 256, 16), (129, 288, 16), (300, 96, 32), (0, 64, 16)])
+def test_scale_atom_bytes(fp4, rows, K, vec):
+    import oracle
+    assert fp4.scale_atom_bytes(rows, K, vec) == oracle.scale_atom_bytes(rows, K // vec)
+
+
+def test_scale_atom_bytes_rejects(fp4):
+    assert fp4.scale_atom_bytes(10, 48, 32) == 0
+    assert fp4.scale_atom_bytes(10, 64, 8) == 0
+    assert fp4.scale_atom_bytes(-1, 64, 16) == 0
+
+
+def _g(fp4, *args, cfg=None):
+    lib = fp4.load()
+    fmt, A, sfA, B, sfB, alpha, D, M, N, K, out = args
+    return lib.fp4_gemm(fmt, 0, A, sfA, B, sfB, alpha, D, M, N, K, out,
+                        ctypes.byref(cfg) if cfg is not None else None, 0)
+
+
+def test_host_validation_without_device(fp4):
+    buf = np.zeros(4096 + 16, np.uint8)
+    p = buf.ctypes.data + (-buf.ctypes.data) % 16          # 16-byte aligned address
+    # empty problems are no-ops
+    assert _g(fp4, 0, p, p, p, p, 1.0, p, 0, 64, 64, 0) == 0
+    assert _g(fp4, 0, p, p, p, p, 1.0, p, 64, 0, 64, 0) == 0
+    # bad enums, sizes and pointers
+    assert _g(fp4, 7, p, p, p, p, 1.0, p, 64, 64, 64, 0) == 1
+    assert _g(fp4, 0, p, p, p, p, 1.0, p, 64, 64, 64, 5) == 1
+    assert _g(fp4, 0, p, p, p, p, 1.0, p, -1, 64, 64, 0) == 1
+    assert _g(fp4, 0, None, p, p, p, 1.0, p, 64, 64, 64, 0) == 1
+    assert _g(fp4, 0, p, p, p, p, 1.0, None, 64, 64, 64, 0) == 1
+    assert _g(fp4, 0, p, p, p, p, 1.0, p, 64, 64, 48, 0) == 2          # K % 32 != 0
+    assert _g(fp4, 0, p + 1, p, p, p, 1.0, p, 64, 64, 64, 0) == 3      # misaligned A
+    assert _g(fp4, 0, p, p, p + 8, p, 1.0, p, 64, 64, 64, 0) == 3      # misaligned B
+    assert _g(fp4, 0, p, p, p, p, 1.0, p + 4, 64, 64, 64, 0) == 3      # misaligned D
+    assert _g(fp4, 0, p, p, p, p, 1.0, p, 1 << 31, 64, 64, 0) == 2     # beyond the index range
+    lib = fp4.load()
+    assert lib.fp4_scale_reorder(p, p, 10, 48, 32, 0) == 2
+    assert lib.fp4_scale_reorder(p, p, -1, 64, 16, 0) == 1
+    assert lib.fp4_scale_reorder(p, p + 4, 10, 64, 16, 0) == 3
+    assert lib.fp4_scale_reorder(p, p, 0, 64, 16, 0) == 0
+    assert lib.fp4_gemm_host(0, p, p, p, p, 1.0, p, 64, 64, 40, 0, 0) == 2
+
+
+def test_python_binding_raises(fp4):
+    buf = np.zeros(64, np.uint8)
+    with pytest.raises(fp4.Fp4Error) as e:
+        fp4.gemm("nvfp4", buf, buf, buf, buf, 1.0, buf, 4, 4, 48, "f32", stream=0)
+    assert e.value.status == 2
+
+
+def test_package_fails_loudly_without_library(tmp_path, monkeypatch):
+    import block_scaled_fp4_sfa_gb300 as m
+    monkeypatch.setattr(m, "_lib", None)
+    monkeypatch.setattr(m._build, "LIB", str(tmp_path / "missing.so"))
+    with pytest.raises(ImportError):
+        m.load()

@@ -1,0 +1,289 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle.
+
+Tolerances (written here, applied element by element):
+  fp32 output: |D - ref| <= 1e-5 * |alpha| * sum_k |a_k b_k| + 1e-6
+  bf16 output: |D - bf16(ref)| <= 1 ulp of bf16(ref)
+  scale reorder: bit-exact.
+Small problems are compared in full; the named workloads at full size on
+sampled rows (every column of each, tile edges and the last row included) and
+on sampled (row, column) pairs.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+
+import workloads as W
+from tests._helpers import bf16_bits_to_f64, bf16_ulp, parse_worked_examples
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module")
+def fp4():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import block_scaled_fp4_sfa_gb300 as m
+    m.build()
+    m.load()
+    return m
+
+
+@pytest.fixture(scope="module")
+def orc():
+    import oracle
+    oracle.build()
+    return oracle
+
+
+def _dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def run(fp4, inp, cfg=None, prepacked=False, out_buf=None):
+    """Runs the GEMM on the device; returns D as float64 (fp32 out) or uint16 bits (bf16 out)."""
+    A, sfA, B, sfB = (_dev(getattr(inp, k)) for k in ("A", "sfA", "B", "sfB"))
+    if prepacked:
+        vec = inp.vec
+        pa = torch.empty(fp4.scale_atom_bytes(inp.M, inp.K, vec), dtype=torch.uint8, device="cuda")
+        pb = torch.empty(fp4.scale_atom_bytes(inp.N, inp.K, vec), dtype=torch.uint8, device="cuda")
+        fp4.scale_reorder(sfA, pa, inp.M, inp.K, vec)
+        fp4.scale_reorder(sfB, pb, inp.N, inp.K, vec)
+        sfA, sfB = pa, pb
+    dt = torch.float32 if inp.out == "f32" else torch.bfloat16
+    D = out_buf if out_buf is not None else torch.full((inp.M, inp.N), float("nan"), dtype=dt, device="cuda")
+    fp4.gemm(inp.fmt, A, sfA, B, sfB, inp.alpha, D, inp.M, inp.N, inp.K, inp.out, prepacked=prepacked,
+             config=cfg)
+    st = fp4.get_device_status()
+    assert st == fp4.FP4_OK, fp4.status_string(st)
+    if inp.out == "f32":
+        return D.cpu().numpy().astype(np.float64)
+    return D.view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def check_values(orc, out, got, ref, absd, what=""):
+    """got / ref / absd of the same shape; raises with the first offending element."""
+    if out == "f32":
+        err = np.abs(got - ref)
+        tol = 1e-5 * absd + 1e-6
+        bad = ~(err <= tol)
+    else:
+        refb = orc.round_bf16(ref)
+        err = np.abs(bf16_bits_to_f64(got) - bf16_bits_to_f64(refb))
+        tol = bf16_ulp(refb)
+        bad = ~(err <= tol)
+    if bad.any():
+        idx = tuple(np.argwhere(bad)[0])
+        raise AssertionError("%s: %d/%d elements out of tolerance; first at %s: got %r ref %r tol %r"
+                             % (what, int(bad.sum()), bad.size, idx, got[idx], ref[idx], tol[idx]))
+    return float(np.max(err / np.maximum(tol, 1e-300))) if err.size else 0.0
+
+
+def check_full(orc, inp, got, what=""):
+    ref, absd = orc.gemm_rows(inp)
+    return check_values(orc, inp.out, got, ref, absd, what or inp.name)
+
+
+def sample_rows(M, n_random=8, seed=0, tile=128):
+    rng = np.random.default_rng(seed)
+    rows = {0, 1, M - 1, M - 2}
+    for edge in range(tile, M, tile * max(1, (M // tile) // 4)):
+        rows.update({edge - 1, edge})
+    rows.update(rng.integers(0, M, n_random).tolist())
+    return np.array(sorted(r for r in rows if 0 <= r < M), dtype=np.int64)
+
+
+def check_sampled(orc, inp, got, seed=0, n_random=8, n_pairs=4000):
+    rows = sample_rows(inp.M, n_random, seed)
+    ref, absd = orc.gemm_rows(inp, rows)
+    r1 = check_values(orc, inp.out, got[rows], ref, absd, "%s rows" % inp.name)
+    rng = np.random.default_rng(seed + 1)
+    ii = rng.integers(0, inp.M, n_pairs)
+    jj = rng.integers(0, inp.N, n_pairs)
+    ii[:4] = [inp.M - 1, inp.M - 1, 0, inp.M // 2]
+    jj[:4] = [inp.N - 1, 0, inp.N - 1, inp.N - 1]
+    refp, absp = orc.gemm_pairs(inp, ii, jj)
+    r2 = check_values(orc, inp.out, got[ii, jj], refp, absp, "%s pairs" % inp.name)
+    return max(r1, r2)
+
+
+# ---- scale reorder ------------------------------------------------------------------
+
+@pytest.mark.parametrize("rows,K,vec", [(128, 64, 16), (300, 288, 16), (1, 32, 32), (257, 4096, 16),
+                                        (1000, 96, 32), (14336, 4096, 16), (129, 5120, 32)])
+def test_scale_reorder_bit_exact(fp4, orc, rows, K, vec):
+    rng = np.random.default_rng(rows + K)
+    sf = rng.integers(0, 256, (rows, K // vec)).astype(np.uint8)
+    nbytes = fp4.scale_atom_bytes(rows, K, vec)
+    assert nbytes == orc.scale_atom_bytes(rows, K // vec)
+    out = torch.full((nbytes,), 0xAB, dtype=torch.uint8, device="cuda")   # padding must be written
+    fp4.scale_reorder(_dev(sf), out, rows, K, vec)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(out.cpu().numpy(), orc.scale_reorder(sf, rows, K // vec))
+
+
+# ---- small problems, full comparison -------------------------------------------------------
+
+def test_smallest_config_matches(fp4, orc):
+    inp = W.make_config("nvfp4_128x128x256_f32")
+    check_full(orc, inp, run(fp4, inp))
+
+
+def test_worked_examples(fp4, orc):
+    for inp, D in parse_worked_examples():
+        got = run(fp4, inp)
+        np.testing.assert_array_equal(got, D, err_msg=inp.name)
+
+
+@pytest.mark.parametrize("fmt", ["nvfp4", "mxfp4"])
+def test_one_hot_products_exact(fp4, orc, fmt):
+    # one nonzero code per row: every output is 0 or a single exact product,
+    # so any permutation of rows, k or scale bytes shows up as a mismatch
+    rng = np.random.default_rng(3)
+    M, N, K = 256, 256, 1024
+    vec = 16 if fmt == "nvfp4" else 32
+    ka = rng.integers(0, K, M)
+    kb = ka[rng.integers(0, M, N)]
+    kb[::3] = rng.integers(0, K, kb[::3].size)
+    codes_a = np.zeros((M, K), np.uint8)
+    codes_b = np.zeros((N, K), np.uint8)
+    codes_a[np.arange(M), ka] = rng.integers(1, 16, M)
+    codes_b[np.arange(N), kb] = rng.integers(1, 16, N)
+    lo, hi = (0x20, 0x60) if fmt == "nvfp4" else (118, 138)
+    sfA = rng.integers(lo, hi, (M, K // vec)).astype(np.uint8)
+    sfB = rng.integers(lo, hi, (N, K // vec)).astype(np.uint8)
+    inp = W.GemmInputs(fmt, M, N, K, W.pack_codes(codes_a), sfA, W.pack_codes(codes_b), sfB, 1.0, "f32", "onehot")
+    ref, _ = orc.gemm_rows(inp)
+    for cfg in (None, fp4.GemmConfig(mode=2, bn=256)):
+        got = run(fp4, inp, cfg)
+        np.testing.assert_array_equal(got, ref)
+
+
+@pytest.mark.parametrize("fmt", ["nvfp4", "mxfp4"])
+@pytest.mark.parametrize("out", ["f32", "bf16"])
+def test_uniform_codes_several_tiles(fp4, orc, fmt, out):
+    inp = W.make_uniform_codes(fmt, 384, 640, 1280, out=out, alpha=0.75, seed=11)
+    check_full(orc, inp, run(fp4, inp))
+
+
+PLAN_CASES = [
+    # (mode, bn, splits): direct with both tile widths, swap-AB with every width, split-K
+    (1, 256, 0), (1, 128, 0), (2, 256, 0), (2, 128, 0), (2, 256, 3), (2, 128, 2),
+]
+
+
+@pytest.mark.parametrize("seed", range(24))
+def test_fuzz_small_shapes(fp4, orc, seed):
+    rng = np.random.default_rng(1000 + seed)
+    fmt = ["nvfp4", "mxfp4"][seed % 2]
+    out = ["f32", "bf16"][(seed // 2) % 2]
+    M = int(rng.integers(1, 301))
+    N = int(rng.integers(1, 301))
+    if out == "bf16":
+        N += (-N) % 8 if seed % 3 else 0       # aligned rows for TMA stores half the time
+    K = int(rng.integers(1, 33)) * 32
+    dist = "t3" if seed % 3 == 0 else "normal"
+    inp = W.make_random(fmt, M, N, K, dist=dist, alpha=float(rng.choice([1.0, 0.5, 3.0])), out=out, seed=seed)
+    check_full(orc, inp, run(fp4, inp), "auto plan")
+    mode, bn, splits = PLAN_CASES[seed % len(PLAN_CASES)]
+    esize = 4 if out == "f32" else 2
+    rows_b = N if mode == 1 else M
+    if mode == 1 and (N * esize) % 16:
+        mode = 2
+        rows_b = M
+    if rows_b > bn and bn < 128:
+        bn = 256
+    cfg = fp4.GemmConfig(mode=mode, bn=bn, splits=splits)
+    check_full(orc, inp, run(fp4, inp, cfg), "plan %s" % ((mode, bn, splits),))
+
+
+@pytest.mark.parametrize("M", [1, 7, 16, 33, 64, 100, 128, 200, 256])
+def test_skinny_swap_widths(fp4, orc, M):
+    inp = W.make_random("nvfp4", M, 1000, 512, out="bf16", seed=M)
+    check_full(orc, inp, run(fp4, inp))
+    check_full(orc, inp, run(fp4, inp, fp4.GemmConfig(mode=2, splits=2)), "split 2")
+
+
+def test_k_tail_not_multiple_of_tile(fp4, orc):
+    for K in (32, 96, 288, 544, 800):
+        for fmt in ("nvfp4", "mxfp4"):
+            inp = W.make_random(fmt, 130, 136, K, out="f32", seed=K)
+            check_full(orc, inp, run(fp4, inp), "K=%d %s" % (K, fmt))
+            check_full(orc, inp, run(fp4, inp, fp4.GemmConfig(mode=2, bn=256)), "K=%d %s swap" % (K, fmt))
+
+
+def test_prepacked_equals_plain(fp4, orc):
+    inp = W.make_random("mxfp4", 300, 520, 768, out="f32", seed=4)
+    a = run(fp4, inp)
+    b = run(fp4, inp, prepacked=True)
+    np.testing.assert_array_equal(a, b)
+
+
+def test_deterministic_bytes(fp4, orc):
+    inp = W.make_random("nvfp4", 700, 1100, 2048, out="bf16", seed=5)
+    a = run(fp4, inp)
+    b = run(fp4, inp)
+    np.testing.assert_array_equal(a, b)
+    c = run(fp4, inp, fp4.GemmConfig(mode=2, splits=4))
+    d = run(fp4, inp, fp4.GemmConfig(mode=2, splits=4))
+    np.testing.assert_array_equal(c, d)
+
+
+def test_persistent_grid_cap(fp4, orc):
+    # few CTAs, many tiles each: exercises the stage / accumulator phase wrap-around
+    inp = W.make_random("nvfp4", 1024, 1024, 1024, out="f32", seed=6)
+    for cfg in (fp4.GemmConfig(max_ctas=3), fp4.GemmConfig(mode=2, bn=128, max_ctas=2),
+                fp4.GemmConfig(mode=1, bn=128, max_ctas=1)):
+        check_full(orc, inp, run(fp4, inp, cfg), "cap")
+
+
+# ---- the named workloads at full size, sampled -------------------------------------------
+
+SAMPLED = [n for n in W.config_names() if n != "nvfp4_128x128x256_f32"]
+
+
+@pytest.mark.parametrize("name", SAMPLED)
+def test_named_workload_sampled(fp4, orc, name):
+    inp = W.make_config(name)
+    got = run(fp4, inp)
+    assert np.isfinite(got).all() if inp.out == "f32" else True
+    check_sampled(orc, inp, got, n_random=4 if inp.M * inp.N * inp.K > 2 ** 36 else 8)
+
+
+# ---- the host-buffer path, empty and degenerate calls -----------------------------------------
+
+def test_host_buffers(fp4, orc):
+    inp = W.make_random("nvfp4", 200, 264, 640, out="bf16", seed=8)
+    D = np.full((inp.M, inp.N), 0x7FC0, np.uint16)
+    A, sfA, B, sfB = (np.ascontiguousarray(getattr(inp, k)) for k in ("A", "sfA", "B", "sfB"))
+    fp4.gemm_host(inp.fmt, A, sfA, B, sfB, inp.alpha, D, inp.M, inp.N, inp.K, inp.out)
+    torch.cuda.synchronize()
+    check_full(orc, inp, D)
+
+
+def test_empty_and_k_zero(fp4):
+    D = torch.full((4, 8), 7.0, device="cuda")
+    z = torch.zeros(16, dtype=torch.uint8, device="cuda")
+    assert fp4.gemm("nvfp4", z, z, z, z, 1.0, D, 0, 8, 64, "f32") == 0
+    assert fp4.gemm("nvfp4", z, z, z, z, 1.0, D, 4, 0, 64, "f32") == 0
+    torch.cuda.synchronize()
+    assert (D == 7.0).all()
+    fp4.gemm("nvfp4", None, None, None, None, 1.0, D, 4, 8, 0, "f32")
+    torch.cuda.synchronize()
+    assert (D == 0.0).all()
+
+
+def test_error_statuses_launch_nothing(fp4):
+    z = torch.zeros(4096, dtype=torch.uint8, device="cuda")
+    D = torch.zeros(64, 64, device="cuda")
+    g = lambda *a, **k: fp4.gemm(*a, check=False, **k)
+    assert g("nvfp4", z, z, z, z, 1.0, D, 64, 64, 48, "f32") == 2            # K % 32
+    assert g("nvfp4", z, z, z, z, 1.0, D, -1, 64, 64, "f32") == 1
+    assert g("nvfp4", None, z, z, z, 1.0, D, 64, 64, 64, "f32") == 1
+    assert g("nvfp4", z[1:], z, z, z, 1.0, D, 64, 64, 64, "f32") == 3         # misaligned A
+    assert g("nvfp4", z, z, z, z, 1.0, D, 64, 64, 64, "f32", config=fp4.GemmConfig(mode=1, bn=64)) == 2
+    assert g("nvfp4", z, z, z, z, 1.0, D, 64, 64, 64, "f32", config=fp4.GemmConfig(mode=1, splits=2)) == 2
+    assert g("nvfp4", z, z, z, z, 1.0, D, 64, 64, 64, "f32", config=fp4.GemmConfig(bn=48)) == 1
+    assert fp4.get_device_status() == 0
