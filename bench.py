@@ -7,7 +7,8 @@ A step is one pass of the whole hot path over one problem: the scale reorder
 of sfA and sfB into the 128x4 atom layout, then the persistent tcgen05 GEMM on
 the reordered scales -- exactly what fp4_gemm_nvfp4 / fp4_gemm_mxfp4 launch --
 each a C-ABI call. Inputs are seeded synthetic data resident in HBM; L2 is
-flushed (a 256 MiB write) between timed steps, outside each step's events.
+flushed (a 256 MiB write) between timed steps, outside each step's events, and
+a spin kernel queued before each step keeps host launch overhead out of them.
 
 `value` is whole-job TFLOP/s (2*M*N*K per step, summed over ranks, divided by
 the slowest rank's time). `roofline` is for the GEMM kernel: its FLOPs per
@@ -48,6 +49,7 @@ FP4_PER_BF16 = 13.5 / 2.25       # nominal dense FP4 : dense bf16 tensor through
 FALLBACK_BF16_TFLOPS = 1900.0
 FALLBACK_HBM_GBS = 6800.0
 L2_FLUSH_BYTES = 256 << 20
+SPACER_CYCLES = 400_000          # ~0.2 ms at 2 GHz
 
 
 def log(*a):
@@ -105,6 +107,8 @@ class ClockSampler:
         self.proc = None
 
     def __enter__(self):
+        if self.index < 0:
+            return self
         try:
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.Q,
                                           "--format=csv,noheader,nounits", "-lms", "100"],
@@ -184,6 +188,21 @@ def run_reference(args, inp):
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+def slowest_rank_ms(local_ms, world_size, device=None):
+    """Max over ranks of the timed-region milliseconds (replicas run concurrently)."""
+    if world_size <= 1:
+        return float(local_ms)
+    import torch
+    t = torch.tensor([float(local_ms)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(flops_per_step, steps, world_size, total_ms):
+    """Units all ranks processed (every rank runs `steps` steps) over the slowest rank's time."""
+    return flops_per_step * steps * world_size / (total_ms * 1e-3) / 1e12
+
+
 def workload_config(inp):
     return {"workload": inp.name, "format": inp.fmt, "M": inp.M, "N": inp.N, "K": inp.K, "out": inp.out,
             "alpha": inp.alpha, "l2": "flushed between steps (256 MiB write, outside the step events)"}
@@ -208,6 +227,11 @@ def run_ours(args, inp, rank, ws, local):
     prepacked = fp4.gemm_nvfp4_prepacked if inp.fmt == "nvfp4" else fp4.gemm_mxfp4_prepacked
     s = stream.cuda_stream
 
+    def spacer():
+        # a spin kernel keeps the GPU busy while the host enqueues the step, so no
+        # host launch overhead falls between the events that bracket the kernels
+        torch.cuda._sleep(SPACER_CYCLES)
+
     def step():
         fp4.scale_reorder(sfA, atomA, inp.M, inp.K, vec, stream=s)
         fp4.scale_reorder(sfB, atomB, inp.N, inp.K, vec, stream=s)
@@ -219,6 +243,7 @@ def run_ours(args, inp, rank, ws, local):
     ev_g1 = torch.cuda.Event(enable_timing=True)
     for _ in range(args.warmup):
         flush.zero_()
+        spacer()
         step()
     torch.cuda.synchronize()
     st = fp4.get_device_status(s)
@@ -232,11 +257,12 @@ def run_ours(args, inp, rank, ws, local):
     if ws > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
-    with ClockSampler(local) as clk:
+    with ClockSampler(local if not args.quick else -1) as clk:
         time.sleep(0.2)
         t_wall0 = time.perf_counter()
         for i in range(args.steps):
             flush.zero_()
+            spacer()
             starts[i].record(stream)
             ev_g0, ev_g1 = g0[i], g1[i]
             step()
@@ -250,13 +276,14 @@ def run_ours(args, inp, rank, ws, local):
         raise RuntimeError("device status after timing: %s" % fp4.status_string(st))
     step_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
     gemm_ms = [a.elapsed_time(b) for a, b in zip(g0, g1)]
-    total_ms = sum(step_ms)
-    if ws > 1:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = slowest_rank_ms(sum(step_ms), ws, dev)
     ms_per_step = total_ms / args.steps
-    value = inp.flops * args.steps * ws / (total_ms * 1e-3) / 1e12
+    value = whole_job_tflops(inp.flops, args.steps, ws, total_ms)
+
+    result_quick = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "ms_per_step": ms_per_step,
+                    "gemm_us": 1e3 * sum(gemm_ms) / len(gemm_ms), "config": workload_config(inp)}
+    if args.quick:
+        return result_quick
 
     # e2e: host buffers through fp4_gemm_host, pinned memory, copies inside the timed region
     pA, psA, pB, psB = (t.pin_memory() for t in (hA, hsA, hB, hsB))
@@ -314,6 +341,8 @@ def main():
     ap.add_argument("--ref-step-s", type=float, default=3.0, help="oracle seconds per reference step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--results", default=None, help="also append the JSON line to this file")
+    ap.add_argument("--quick", action="store_true",
+                    help="GEMM steps only: no e2e, clock or CPU legs (for profiling runs)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -331,7 +360,7 @@ def main():
             torch.distributed.init_process_group("nccl")
         inp = W.make_config(args.workload)
         res = run_ours(args, inp, rank, ws, local)
-        if rank == 0 and not args.no_cpu_baseline:
+        if rank == 0 and not args.no_cpu_baseline and not args.quick:
             rows = cpu_sample_rows(inp, args.cpu_sample_s)
             v, dt = oracle_rows_tflops(inp, rows)
             res["cpu_baseline"] = {"value": v, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
