@@ -38,7 +38,7 @@ class Fp4Error(RuntimeError):
 class GemmConfig(ctypes.Structure):
     """fp4_gemm_config: plan overrides (0 = automatic)."""
     _fields_ = [("mode", ctypes.c_int32), ("bn", ctypes.c_int32), ("splits", ctypes.c_int32),
-                ("max_ctas", ctypes.c_int32)]
+                ("max_ctas", ctypes.c_int32), ("cta_group", ctypes.c_int32)]
 
 
 def build(force: bool = False) -> str:

@@ -10,29 +10,35 @@
 // E8M0 scale per 32 ("TMA Pipelines, Tensor Cores, and ctm-rs Interop",
 // section 1). The kernel is a persistent, warp-specialised tcgen05 GEMM:
 //
-//   warp 0      TMA producer: fills a ring of shared-memory stages, each one
-//               k-tile (256 FP4 elements = 128 bytes per row) of the two
-//               operands (128B-swizzled) plus their scale atoms;
-//   warp 1      MMA issuer: one thread copies the scale atoms into TMEM
-//               (tcgen05.cp) and issues four K=64 block-scaled MMAs per k-tile
-//               into a TMEM accumulator, then releases the stage;
-//   warps 2..5  epilogue: TMEM -> registers (tcgen05.ld), * alpha, cast,
-//               then either a swizzled shared tile + TMA store, or coalesced
-//               direct stores of the transposed tile (swap-AB), or fp32
-//               split-K partials.
+//   warp 0      TMA producer (one thread): fills a ring of shared-memory
+//               stages; a stage is one k-tile (256 FP4 elements = 128 bytes
+//               per row) of both operands (128B-swizzled) and their scale atoms;
+//   warp 1      MMA issuer (one thread of the leader CTA): copies the stage's
+//               scale atoms into TMEM (tcgen05.cp) and issues four K = 64
+//               block-scaled MMAs into a TMEM accumulator, then frees the stage;
+//   warps 2..9  epilogue: each warp drains its 32 TMEM lanes x BN/2 columns
+//               into registers, hands the accumulator back at once, then
+//               scales, casts and stores (a per-warp 128B-swizzled TMA store
+//               box, coalesced stores of the transposed tile for swap-AB, or
+//               fp32 split-K partials) while the next tile's MMAs run.
 //
-// The warp roles follow the split shown for the SM100a two-CTA kernel in
-// "TMA Pipelines, Tensor Cores, and ctm-rs Interop", section 2 (producer warp,
-// single-thread MMA warp, epilogue warps draining TMEM); the K-tile of four MMA
+// CG = 2 runs a CTA pair (cluster of 2) on one 256-row MMA (tcgen05
+// cta_group::2): each CTA loads 128 rows of the M side and half of the N side,
+// the leader issues the MMAs, and each CTA's TMEM holds its 128 rows of D.
+//
+// The warp roles follow the SM100a two-CTA kernel in "TMA Pipelines, Tensor
+// Cores, and ctm-rs Interop", section 2 (producer warp, single-thread MMA
+// warp, epilogue warps draining TMEM, paired CTAs); the K-tile of four MMA
 // instructions and the 128-byte swizzle follow "Hopper GEMM in CUTLASS C++ and
-// the CuTe DSL, part 1" (the K extent of the tile is four MMA instructions;
-// the widest swizzle atom that divides the tile's K bytes is taken).
+// the CuTe DSL, part 1" (tile K = four MMA instructions; the widest swizzle atom
+// dividing the tile's K bytes), as does the stage count (shared capacity minus
+// the epilogue carve-out, over the bytes of one stage).
 //
-// "Slot A" is the operand on the MMA's 128-row M side, "slot B" the one on its
-// N side. Direct mode: slot A = A, slot B = B. Swap-AB mode: slot A = B, slot
-// B = A, and the epilogue writes D^T tiles into row-major D -- the swapped
-// operands of the W4A8 kernel in "Hopper GEMM in CUTLASS C++ and the CuTe DSL,
-// part 1" ("The operands are swapped").
+// "Slot A" is the operand on the MMA's M side, "slot B" the one on its N side.
+// Direct mode: slot A = A, slot B = B. Swap-AB mode: slot A = B, slot B = A,
+// and the epilogue writes D^T tiles into row-major D -- the swapped operands of
+// "Hopper GEMM in CUTLASS C++ and the CuTe DSL, part 1" ("The operands are
+// swapped").
 
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -53,53 +59,49 @@ namespace fp4 {
 // Per-device status word: 0, or the first error a kernel recorded.
 __device__ int g_status;
 
-constexpr int kBM = 128;          // MMA M (cta_group::1)
+constexpr int kBM = 128;          // TMEM lanes / M rows per CTA
 constexpr int kBK = 256;          // FP4 elements per k-tile
 constexpr int kBKBytes = 128;     // bytes per row per k-tile
-constexpr int kMmaK = 64;         // FP4 elements per block-scaled MMA
 constexpr int kAtomBytes = 512;   // one 128-row x 4-column scale atom
-constexpr int kSfChunk = 2048;    // shared bytes per 128-row scale block per stage (4 atoms)
-constexpr int kThreads = 192;     // producer warp, MMA warp, 4 epilogue warps
-constexpr int kEpiThreads = 128;
+constexpr int kEpiWarps = 8;
+constexpr int kThreads = 64 + 32 * kEpiWarps;   // producer warp, MMA warp, epilogue warps
+constexpr int kStgBytes = 32 * 128;             // per-warp store box: 32 rows x 128 bytes
 constexpr int kSmemLimit = 232448;
 
 enum EpiMode : int32_t { kEpiTmaStore = 0, kEpiTransposed = 1, kEpiSplitK = 2 };
 
 struct Args {
-    const uint8_t *sfa;      // atom-layout scales of slot A
-    const uint8_t *sfb;      // atom-layout scales of slot B
     void *out;               // D (modes 0, 1) or split-K workspace (mode 2)
     int64_t ldo;             // row stride in elements of `out` for modes 1 and 2
     int64_t split_stride;    // elements between split partials (mode 2)
     uint64_t wait_ns;        // bound on every mbarrier wait
-    int32_t rows_a, rows_b, K;
-    int32_t kc4;             // scale atoms per 128-row block along K
+    int32_t rows_a, rows_b;
     int32_t k_tiles;         // ceil(K / 256)
     int32_t kps;             // k-tiles per split
     int32_t tiles_a, tiles_b, splits, units, group_b;
-    int32_t mx;              // 0 NVFP4 (vec 16, UE4M3), 1 MXFP4 (vec 32, UE8M0)
     int32_t bf16;            // output type for modes 0 and 1
     int32_t mode;            // EpiMode
     float alpha;
 };
 
-template <int BN>
+template <int CG, int BN, bool MX>
 struct Cfg {
-    static constexpr int NRB = (BN + 127) / 128;              // 128-row scale blocks on the N side
-    static constexpr int A_BYTES = kBM * kBKBytes;             // 16 KB
-    static constexpr int B_BYTES = BN * kBKBytes;
-    static constexpr int SFA_BYTES = kSfChunk;
-    static constexpr int SFB_BYTES = NRB * kSfChunk;
+    static constexpr int APK = MX ? 2 : 4;             // scale atoms per k-tile per 128-row block
+    static constexpr int NRB = (BN + 127) / 128;       // 128-row scale blocks on the N side (whole tile)
+    static constexpr int BN_CTA = BN / CG;             // N-side rows loaded by one CTA
+    static constexpr int A_BYTES = kBM * kBKBytes;      // 16 KB
+    static constexpr int B_BYTES = BN_CTA * kBKBytes;
+    static constexpr int SFA_BYTES = APK * kAtomBytes;
+    static constexpr int SFB_BYTES = NRB * APK * kAtomBytes;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
-    static constexpr bool TMA_EPI = BN >= 128;                 // direct mode needs the store staging
-    static constexpr int STAGING_BYTES = TMA_EPI ? 2 * kBM * 128 : 0;
+    static constexpr int STAGING_BYTES = kEpiWarps * kStgBytes;
     static constexpr int BAR_BYTES = 256;
-    static constexpr int BUDGET = kSmemLimit - 1024 - BAR_BYTES;
-    static constexpr int STAGES_FIT = (BUDGET - STAGING_BYTES) / STAGE_BYTES;
+    static constexpr int BUDGET = kSmemLimit - 1024 - BAR_BYTES - STAGING_BYTES;
+    static constexpr int STAGES_FIT = BUDGET / STAGE_BYTES;
     static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
     static constexpr int ACC_BUFS = BN <= 128 ? 2 : 1;
-    // TMEM per stage: SFA 4 atoms x 4 columns, SFB 4 atoms x 4 columns per row block.
-    static constexpr int SF_COLS = 16 + NRB * 16;
+    static constexpr int SF_COLS = 4 * APK * (1 + NRB);   // TMEM columns of one stage's scales
+    static constexpr int SF_TMEM = ACC_BUFS * BN;          // first scale column
     static constexpr int TMEM_USED = ACC_BUFS * BN + STAGES * SF_COLS;
     static constexpr int TMEM_COLS = TMEM_USED <= 32 ? 32 : TMEM_USED <= 64 ? 64 : TMEM_USED <= 128 ? 128
                                    : TMEM_USED <= 256 ? 256 : 512;
@@ -110,10 +112,15 @@ struct Cfg {
     static constexpr int OFF_STG = OFF_SFB + STAGES * SFB_BYTES;
     static constexpr int OFF_BAR = OFF_STG + STAGING_BYTES;
     static constexpr int SMEM_BYTES = OFF_BAR + BAR_BYTES + 1024;   // + alignment slack
+    static constexpr int COLS_WARP = BN / 2;                        // accumulator columns per epilogue warp
+    static constexpr uint32_t TX_BYTES = CG * STAGE_BYTES;          // bytes landing per stage (both CTAs)
+    static_assert(CG == 1 || CG == 2, "CTA group of 1 or 2");
+    static_assert(CG == 1 || BN >= 128, "paired CTAs use N tiles of 128 or 256");
     static_assert(STAGES >= 2, "too few pipeline stages");
     static_assert(TMEM_USED <= 512, "TMEM budget exceeded");
     static_assert(SMEM_BYTES <= kSmemLimit, "shared memory budget exceeded");
     static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N must be a multiple of 16 in [16, 256]");
+    static_assert(OFF_STG % 1024 == 0 && kStgBytes % 1024 == 0, "swizzled staging must be 1024-aligned");
 };
 
 // Records the first error of this device (later ones are dropped).
@@ -122,13 +129,12 @@ __device__ __forceinline__ void record_error(int code)
     atomicCAS(&g_status, 0, code);
 }
 
-// mbarrier wait with a time bound. On expiry it records FP4_ERR_TIMEOUT in the
-// device status word, raises this CTA's abort flag and returns false; it also
-// gives up early once another role of the CTA raised the flag.
-__device__ __noinline__ bool wait_bounded(uint32_t bar, uint32_t parity, uint64_t limit_ns,
-                                          volatile uint32_t *abort_flag)
+// Slow path of wait(): polls with a time bound. On expiry it records
+// FP4_ERR_TIMEOUT in the device status word, raises this CTA's abort flag and
+// returns false; it also gives up once another role of the CTA raised the flag.
+__device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, uint64_t limit_ns,
+                                       volatile uint32_t *abort_flag)
 {
-    if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
@@ -141,6 +147,13 @@ __device__ __noinline__ bool wait_bounded(uint32_t bar, uint32_t parity, uint64_
             }
         }
     }
+}
+
+__device__ __forceinline__ bool wait(uint32_t bar, uint32_t parity, uint64_t limit_ns,
+                                     volatile uint32_t *abort_flag)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    return wait_slow(bar, parity, limit_ns, abort_flag);
 }
 
 // Unit u -> (slot-A tile, slot-B tile, split). Splits are outermost; inside a
@@ -160,12 +173,33 @@ __device__ __forceinline__ void unit_coords(const Args &a, int u, int &ta, int &
     ta = r / gw;
 }
 
-template <int BN>
+// Loads N consecutive 32-bit TMEM columns of this warp's 32 lanes.
+template <int N>
+__device__ __forceinline__ void tmem_load_cols(uint32_t taddr, uint32_t *v)
+{
+    if constexpr (N == 8) {
+        uint32_t (&r)[8] = *reinterpret_cast<uint32_t(*)[8]>(v);
+        tmem_ld_32x32b_x8(taddr, r);
+    } else if constexpr (N == 16) {
+        uint32_t (&r)[16] = *reinterpret_cast<uint32_t(*)[16]>(v);
+        tmem_ld_32x32b_x16(taddr, r);
+    } else {
+        static_assert(N % 32 == 0, "column count");
+#pragma unroll
+        for (int c = 0; c < N / 32; ++c) {
+            uint32_t (&r)[32] = *reinterpret_cast<uint32_t(*)[32]>(v + 32 * c);
+            tmem_ld_32x32b_x32(taddr + 32 * c, r);
+        }
+    }
+}
+
+template <int CG, int BN, bool MX>
 __global__ void __launch_bounds__(kThreads, 1)
     fp4_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
+                    const __grid_constant__ CUtensorMap tmap_sfa, const __grid_constant__ CUtensorMap tmap_sfb,
                     const __grid_constant__ CUtensorMap tmap_d, const Args args)
 {
-    using C = Cfg<BN>;
+    using C = Cfg<CG, BN, MX>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -182,6 +216,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
+    const uint32_t rank = CG == 2 ? cluster_ctarank() : 0u;   // 0 = leader of the pair
+    const int pair = CG == 2 ? static_cast<int>(blockIdx.x / 2) : static_cast<int>(blockIdx.x);
+    const int npairs = CG == 2 ? static_cast<int>(gridDim.x / 2) : static_cast<int>(gridDim.x);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::STAGES; ++s) {
@@ -190,7 +227,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(bar_acc_full + 8 * b, 1);
-            mbar_init(bar_acc_empty + 8 * b, kEpiThreads);
+            mbar_init(bar_acc_empty + 8 * b, kEpiWarps * CG);
         }
         mbar_init(bar_drain, 1);
         *abort_flag = 0;
@@ -199,54 +236,51 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 32) {
         prefetch_tensormap(&tmap_a);
         prefetch_tensormap(&tmap_b);
+        prefetch_tensormap(&tmap_sfa);
+        prefetch_tensormap(&tmap_sfb);
         if (args.mode == kEpiTmaStore) prefetch_tensormap(&tmap_d);
     }
     if (warp == 1) {
-        tmem_alloc(smem_u32(tmem_holder), C::TMEM_COLS);
-        tmem_relinquish();
+        tmem_alloc<CG>(smem_u32(tmem_holder), C::TMEM_COLS);
+        tmem_relinquish<CG>();
     }
     tc_fence_before();
-    __syncthreads();
+    if constexpr (CG == 2) cluster_sync(); else __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
-
-    const int apk = args.mx ? 2 : 4;   // scale atoms per k-tile (per 128-row block)
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
+            // every CTA signals the leader's full barrier; the leader posts the
+            // byte count of both CTAs
+            const uint32_t full0 = CG == 2 ? mapa_shared(bar_full, 0) : bar_full;
             int stage = 0;
             uint32_t phase = 0;
-            uint32_t filled = 0;                   // bit s: stage s has a fill in flight
-            uint32_t fill_parity = 0;              // bit s: parity of that fill
+            uint32_t filled = 0, fill_parity = 0;
             bool ok = true;
-            const int rbb_count = (args.rows_b + 127) / 128;
-            for (int u = blockIdx.x; ok && u < args.units; u += gridDim.x) {
+            for (int u = pair; ok && u < args.units; u += npairs) {
                 int ta, tb, split;
                 unit_coords(args, u, ta, tb, split);
                 const int kt0 = split * args.kps;
                 const int kt1 = min(kt0 + args.kps, args.k_tiles);
-                const int row_a0 = ta * kBM, row_b0 = tb * BN;
-                const int rbb0 = row_b0 / 128;
-                const int nrb = min(C::NRB, rbb_count - rbb0);
+                const int rba = ta * CG + static_cast<int>(rank);       // this CTA's 128-row block of slot A
+                const int row_a = rba * kBM;
+                const int row_b = tb * BN + static_cast<int>(rank) * C::BN_CTA;
+                const int rbb = (tb * BN) / 128;                         // first scale block of the N side
                 for (int kt = kt0; kt < kt1; ++kt) {
-                    if (!wait_bounded(bar_empty + 8 * stage, phase ^ 1u, args.wait_ns, abort_flag)) {
+                    if (!wait(bar_empty + 8 * stage, phase ^ 1u, args.wait_ns, abort_flag)) {
                         ok = false;
                         break;
                     }
-                    const int atoms = min(apk, args.kc4 - kt * apk);
-                    const uint32_t sf_bytes = static_cast<uint32_t>(atoms) * kAtomBytes;
-                    const uint32_t full = bar_full + 8 * stage;
-                    mbar_arrive_expect_tx(full, C::A_BYTES + C::B_BYTES + sf_bytes * (1 + nrb));
-                    tma_load_2d(base + C::OFF_A + stage * C::A_BYTES, &tmap_a, full, kt * kBKBytes, row_a0);
-                    tma_load_2d(base + C::OFF_B + stage * C::B_BYTES, &tmap_b, full, kt * kBKBytes, row_b0);
-                    bulk_load(base + C::OFF_SFA + stage * C::SFA_BYTES,
-                              args.sfa + (static_cast<int64_t>(ta) * args.kc4 + kt * apk) * kAtomBytes,
-                              sf_bytes, full);
-                    for (int rb = 0; rb < nrb; ++rb)
-                        bulk_load(base + C::OFF_SFB + stage * C::SFB_BYTES + rb * kSfChunk,
-                                  args.sfb + (static_cast<int64_t>(rbb0 + rb) * args.kc4 + kt * apk) * kAtomBytes,
-                                  sf_bytes, full);
+                    const uint32_t full = full0 + 8 * stage;                 // shared::cluster address
+                    if (rank == 0) mbar_arrive_expect_tx(bar_full + 8 * stage, C::TX_BYTES);
+                    tma_load_2d<CG>(base + C::OFF_A + stage * C::A_BYTES, &tmap_a, full, kt * kBKBytes, row_a);
+                    tma_load_2d<CG>(base + C::OFF_B + stage * C::B_BYTES, &tmap_b, full, kt * kBKBytes, row_b);
+                    tma_load_2d<CG>(base + C::OFF_SFA + stage * C::SFA_BYTES, &tmap_sfa, full,
+                                    kt * C::APK * (kAtomBytes / 8), rba);
+                    tma_load_2d<CG>(base + C::OFF_SFB + stage * C::SFB_BYTES, &tmap_sfb, full,
+                                    kt * C::APK * (kAtomBytes / 8), rbb);
                     filled |= 1u << stage;
                     fill_parity = (fill_parity & ~(1u << stage)) | (phase << stage);
                     if (++stage == C::STAGES) {
@@ -255,71 +289,73 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
-            // Let every copy this thread started land before the CTA can exit.
-            for (int s = 0; s < C::STAGES; ++s)
-                if (filled & (1u << s)) wait_bounded(bar_full + 8 * s, (fill_parity >> s) & 1u, args.wait_ns, abort_flag);
+            // The leader lets every copy it waited for land before the CTA can exit;
+            // the peer's copies signal the leader, whose MMA warp waits for them.
+            if (rank == 0)
+                for (int s = 0; s < C::STAGES; ++s)
+                    if (filled & (1u << s)) wait(bar_full + 8 * s, (fill_parity >> s) & 1u, args.wait_ns, abort_flag);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
+        if (lane == 0 && rank == 0) {
+            // Instruction descriptors: MXFP4 alternates the scale byte ids 0 / 2
+            // between the two K=64 halves of one 4-block atom.
+            constexpr uint32_t ID0 = idesc_fp4(kBM * CG, BN, MX, 0, 0);
+            constexpr uint32_t ID2 = idesc_fp4(kBM * CG, BN, MX, 2, 2);
+            // K-major, 128-byte swizzle: rows 128 bytes apart, 8-row groups 1024
+            // apart; MMA j of a k-tile starts 32 bytes (two 16-byte units) in.
+            const uint64_t desc_a0 = smem_desc(base + C::OFF_A, 16, 1024, 2);
+            const uint64_t desc_b0 = smem_desc(base + C::OFF_B, 16, 1024, 2);
+            // A scale atom: 32 rows of 16 bytes, 8-row groups 128 bytes apart.
+            const uint64_t desc_sfa0 = smem_desc(base + C::OFF_SFA, 0, 128, 0);
+            const uint64_t desc_sfb0 = smem_desc(base + C::OFF_SFB, 0, 128, 0);
             int stage = 0;
             uint32_t phase = 0;
             int acc = 0;
             uint32_t acc_phase = 0;
             bool ok = true;
-            const bool mx = args.mx != 0;
-            for (int u = blockIdx.x; ok && u < args.units; u += gridDim.x) {
+            for (int u = pair; ok && u < args.units; u += npairs) {
                 int ta, tb, split;
                 unit_coords(args, u, ta, tb, split);
                 const int kt0 = split * args.kps;
                 const int kt1 = min(kt0 + args.kps, args.k_tiles);
-                if (!wait_bounded(bar_acc_empty + 8 * acc, acc_phase ^ 1u, args.wait_ns, abort_flag)) break;
+                if (!wait(bar_acc_empty + 8 * acc, acc_phase ^ 1u, args.wait_ns, abort_flag)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem + static_cast<uint32_t>(acc * BN);
                 for (int kt = kt0; kt < kt1; ++kt) {
-                    if (!wait_bounded(bar_full + 8 * stage, phase, args.wait_ns, abort_flag)) {
+                    if (!wait(bar_full + 8 * stage, phase, args.wait_ns, abort_flag)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    // Scale atoms of this k-tile -> this stage's TMEM scale columns.
-                    const uint32_t sf_col = tmem + static_cast<uint32_t>(C::ACC_BUFS * BN + stage * C::SF_COLS);
-                    const uint32_t sfa_smem = base + C::OFF_SFA + stage * C::SFA_BYTES;
-                    const uint32_t sfb_smem = base + C::OFF_SFB + stage * C::SFB_BYTES;
-                    const int atoms = min(apk, args.kc4 - kt * apk);
-                    for (int t = 0; t < atoms; ++t) {
-                        tc_cp_32x128b_warpx4(sf_col + 4 * t, smem_desc(sfa_smem + t * kAtomBytes, 0, 128, 0));
+                    const uint32_t sf = tmem + static_cast<uint32_t>(C::SF_TMEM + stage * C::SF_COLS);
+                    const uint64_t dsa = desc_sfa0 + static_cast<uint64_t>((stage * C::SFA_BYTES) >> 4);
+                    const uint64_t dsb = desc_sfb0 + static_cast<uint64_t>((stage * C::SFB_BYTES) >> 4);
+#pragma unroll
+                    for (int t = 0; t < C::APK; ++t) {
+                        tc_cp_32x128b_warpx4<CG>(sf + 4 * t, dsa + (t * kAtomBytes >> 4));
+#pragma unroll
                         for (int rb = 0; rb < C::NRB; ++rb)
-                            tc_cp_32x128b_warpx4(sf_col + 16 + t * 4 * C::NRB + 4 * rb,
-                                                 smem_desc(sfb_smem + rb * kSfChunk + t * kAtomBytes, 0, 128, 0));
+                            tc_cp_32x128b_warpx4<CG>(sf + 4 * C::APK + 4 * (t * C::NRB + rb),
+                                                     dsb + ((rb * C::APK + t) * kAtomBytes >> 4));
                     }
-                    const int nmma = min(kBK / kMmaK, (args.K - kt * kBK + kMmaK - 1) / kMmaK);
-                    const uint32_t a_smem = base + C::OFF_A + stage * C::A_BYTES;
-                    const uint32_t b_smem = base + C::OFF_B + stage * C::B_BYTES;
-                    for (int j = 0; j < nmma; ++j) {
-                        // K-major, 128-byte swizzle: rows 128 bytes apart, 8-row groups 1024 apart;
-                        // MMA j reads bytes [32 j, 32 j + 32) of every row.
-                        const uint64_t ad = smem_desc(a_smem + 32 * j, 16, 1024, 2);
-                        const uint64_t bd = smem_desc(b_smem + 32 * j, 16, 1024, 2);
-                        const int t = mx ? (j >> 1) : j;
-                        const uint32_t sf_id = mx ? static_cast<uint32_t>((j & 1) * 2) : 0u;
-                        const uint32_t idesc = idesc_fp4(kBM, BN, mx, sf_id, sf_id);
-                        const uint32_t sfa_t = sf_col + 4 * t;
-                        const uint32_t sfb_t = sf_col + 16 + t * 4 * C::NRB;
-                        const uint32_t accumulate = (kt > kt0 || j > 0) ? 1u : 0u;
-                        if (mx)
-                            tc_mma_fp4_vec32(d_tmem, ad, bd, idesc, sfa_t, sfb_t, accumulate);
-                        else
-                            tc_mma_fp4_vec16(d_tmem, ad, bd, idesc, sfa_t, sfb_t, accumulate);
+                    const uint64_t da = desc_a0 + static_cast<uint64_t>((stage * C::A_BYTES) >> 4);
+                    const uint64_t db = desc_b0 + static_cast<uint64_t>((stage * C::B_BYTES) >> 4);
+#pragma unroll
+                    for (int j = 0; j < kBK / 64; ++j) {
+                        const int t = MX ? (j >> 1) : j;
+                        const uint32_t idesc = (MX && (j & 1)) ? ID2 : ID0;
+                        tc_mma_fp4<CG, MX>(d_tmem, da + 2 * j, db + 2 * j, idesc, sf + 4 * t,
+                                           sf + 4 * C::APK + 4 * C::NRB * t, (kt > kt0 || j > 0) ? 1u : 0u);
                     }
-                    tc_commit(bar_empty + 8 * stage);
+                    tc_commit<CG>(bar_empty + 8 * stage);
                     if (++stage == C::STAGES) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
                 if (!ok) break;
-                tc_commit(bar_acc_full + 8 * acc);
+                tc_commit<CG>(bar_acc_full + 8 * acc);
                 if (C::ACC_BUFS == 2) {
                     acc ^= 1;
                     if (acc == 0) acc_phase ^= 1u;
@@ -328,120 +364,95 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             // Every MMA and scale copy this thread issued completes before teardown.
-            tc_commit(bar_drain);
-            wait_bounded(bar_drain, 0, args.wait_ns, abort_flag);
+            tc_commit<CG>(bar_drain, 1);
+            wait(bar_drain, 0, args.wait_ns, abort_flag);
         }
     } else {
         // ------------------------------------------------------------ epilogue
-        const int q = warp & 3;                       // TMEM lane quarter of this warp
-        const int row_in_tile = 32 * q + lane;
-        const bool leader = threadIdx.x == 64;
+        const int q = warp & 3;                          // TMEM lane quarter of this warp
+        const int h = (warp - 2) >> 2;                   // which half of the tile's columns
+        const uint32_t acc_empty0 = CG == 2 ? mapa_shared(bar_acc_empty, 0) : bar_acc_empty;
+        const uint32_t stg = base + C::OFF_STG + (warp - 2) * kStgBytes;
+        uint8_t *const stg_ptr = base_ptr + C::OFF_STG + (warp - 2) * kStgBytes;
         int acc = 0;
         uint32_t acc_phase = 0;
-        int sb = 0;
-        for (int u = blockIdx.x; u < args.units; u += gridDim.x) {
+        for (int u = pair; u < args.units; u += npairs) {
             int ta, tb, split;
             unit_coords(args, u, ta, tb, split);
-            // The four epilogue warps take the same exit decision (they meet at
-            // named barriers below), so the wait's outcome is AND-reduced first.
-            const bool got = wait_bounded(bar_acc_full + 8 * acc, acc_phase, args.wait_ns, abort_flag);
-            if (!named_bar_and(1, kEpiThreads, got)) break;
+            if (!wait(bar_acc_full + 8 * acc, acc_phase, args.wait_ns, abort_flag)) break;
             tc_fence_after();
-            const uint32_t t_base = tmem + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(acc * BN);
-            const int row_a0 = ta * kBM, row_b0 = tb * BN;
-            if (C::TMA_EPI && args.mode == kEpiTmaStore) {
-                // 128 rows x 128 bytes per subtile: 32 fp32 or 64 bf16 columns.
-                const int cw = args.bf16 ? 64 : 32;
-                const int nsub = BN / cw;
-                const int r = row_in_tile;
-                for (int c = 0; c < nsub; ++c) {
-                    uint32_t packed[32];
-                    if (args.bf16) {
-                        uint32_t v0[32], v1[32];
-                        tmem_ld_32x32b_x32(t_base + c * 64, v0);
-                        tmem_ld_32x32b_x32(t_base + c * 64 + 32, v1);
-                        tmem_ld_wait();
+            // Drain this warp's 32 lanes x BN/2 columns, then release the accumulator.
+            uint32_t v[C::COLS_WARP];
+            tmem_load_cols<C::COLS_WARP>(tmem + (static_cast<uint32_t>(32 * q) << 16) +
+                                             static_cast<uint32_t>(acc * BN + h * C::COLS_WARP),
+                                         v);
+            tmem_ld_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                if constexpr (CG == 2)
+                    mbar_arrive_cluster(acc_empty0 + 8 * acc);
+                else
+                    mbar_arrive(bar_acc_empty + 8 * acc);
+            }
+            const int row_a0 = (ta * CG + static_cast<int>(rank)) * kBM + 32 * q;   // this warp's first row
+            const int col0 = tb * BN + h * C::COLS_WARP;
+            if (args.mode == kEpiTmaStore) {
+                if constexpr (C::COLS_WARP >= 64) {
+                    const int cw = args.bf16 ? 64 : 32;                 // columns per 128-byte box row
+                    const int nch = C::COLS_WARP / cw;
+                    for (int ch = 0; ch < nch; ++ch) {
+                        uint32_t w[32];
+                        if (args.bf16) {
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            __nv_bfloat162 h = __floats2bfloat162_rn(__uint_as_float(v0[2 * i]) * args.alpha,
-                                                                     __uint_as_float(v0[2 * i + 1]) * args.alpha);
-                            packed[i] = *reinterpret_cast<uint32_t *>(&h);
-                            __nv_bfloat162 g = __floats2bfloat162_rn(__uint_as_float(v1[2 * i]) * args.alpha,
-                                                                     __uint_as_float(v1[2 * i + 1]) * args.alpha);
-                            packed[16 + i] = *reinterpret_cast<uint32_t *>(&g);
+                            for (int i = 0; i < 32; ++i) {
+                                const int c = ch * 64 + 2 * i;
+                                __nv_bfloat162 p = __floats2bfloat162_rn(__uint_as_float(v[c]) * args.alpha,
+                                                                         __uint_as_float(v[c + 1]) * args.alpha);
+                                w[i] = *reinterpret_cast<uint32_t *>(&p);
+                            }
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < 32; ++i)
+                                w[i] = __float_as_uint(__uint_as_float(v[ch * 32 + i]) * args.alpha);
                         }
-                    } else {
-                        uint32_t v[32];
-                        tmem_ld_32x32b_x32(t_base + c * 32, v);
-                        tmem_ld_wait();
+                        if (lane == 0) bulk_wait_group_read<0>();       // the box buffer is free again
+                        __syncwarp();
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) packed[i] = __float_as_uint(__uint_as_float(v[i]) * args.alpha);
+                        for (int c = 0; c < 8; ++c)
+                            *reinterpret_cast<uint4 *>(stg_ptr + lane * 128 + ((c ^ (lane & 7)) << 4)) =
+                                make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            tma_store_2d(&tmap_d, stg, col0 + ch * cw, row_a0);
+                            bulk_commit_group();
+                        }
                     }
-                    if (c == nsub - 1) {
-                        // the accumulator is fully read: hand it back to the MMA warp
-                        tc_fence_before();
-                        mbar_arrive(bar_acc_empty + 8 * acc);
-                    }
-                    if (leader) bulk_wait_group_read<1>();
-                    named_bar_sync(1, kEpiThreads);
-                    uint8_t *stg = base_ptr + C::OFF_STG + sb * (kBM * 128);
-#pragma unroll
-                    for (int ch = 0; ch < 8; ++ch) {
-                        uint4 w = make_uint4(packed[4 * ch], packed[4 * ch + 1], packed[4 * ch + 2], packed[4 * ch + 3]);
-                        *reinterpret_cast<uint4 *>(stg + r * 128 + ((ch ^ (r & 7)) << 4)) = w;
-                    }
-                    fence_proxy_async_smem();
-                    named_bar_sync(1, kEpiThreads);
-                    if (leader) {
-                        tma_store_2d(&tmap_d, base + C::OFF_STG + sb * (kBM * 128), row_b0 + c * cw, row_a0);
-                        bulk_commit_group();
-                    }
-                    sb ^= 1;
                 }
             } else {
                 // Transposed direct stores (swap-AB) or fp32 split-K partials: for a
-                // fixed TMEM column the 32 lanes of a warp write 32 consecutive elements.
-                const int ra = row_a0 + row_in_tile;
-                const bool row_ok = ra < args.rows_a;
-                constexpr int CH = BN < 32 ? BN : 32;
-                for (int c = 0; c < BN / CH; ++c) {
-                    uint32_t v[32];
-                    if constexpr (CH == 32) {
-                        tmem_ld_32x32b_x32(t_base + c * 32, v);
-                    } else {
-                        uint32_t w[16];
-                        tmem_ld_32x32b_x16(t_base, w);
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) v[i] = w[i];
-                    }
-                    tmem_ld_wait();
-                    if (c == BN / CH - 1) {
-                        tc_fence_before();
-                        mbar_arrive(bar_acc_empty + 8 * acc);
-                    }
-                    if (!row_ok) continue;
+                // fixed column the 32 lanes of a warp write 32 consecutive elements.
+                const int ra = row_a0 + lane;
+                if (ra < args.rows_a) {
                     if (args.mode == kEpiSplitK) {
-                        float *ws = static_cast<float *>(args.out) + split * args.split_stride;
+                        float *ws = static_cast<float *>(args.out) + split * args.split_stride + ra;
 #pragma unroll
-                        for (int i = 0; i < CH; ++i) {
-                            const int rb = row_b0 + c * CH + i;
-                            if (rb < args.rows_b) ws[static_cast<int64_t>(rb) * args.ldo + ra] = __uint_as_float(v[i]);
-                        }
+                        for (int i = 0; i < C::COLS_WARP; ++i)
+                            if (col0 + i < args.rows_b) ws[static_cast<int64_t>(col0 + i) * args.ldo] = __uint_as_float(v[i]);
                     } else if (args.bf16) {
-                        __nv_bfloat16 *d = static_cast<__nv_bfloat16 *>(args.out);
+                        __nv_bfloat16 *d = static_cast<__nv_bfloat16 *>(args.out) + ra;
 #pragma unroll
-                        for (int i = 0; i < CH; ++i) {
-                            const int rb = row_b0 + c * CH + i;
-                            if (rb < args.rows_b)
-                                d[static_cast<int64_t>(rb) * args.ldo + ra] = __float2bfloat16_rn(__uint_as_float(v[i]) * args.alpha);
-                        }
+                        for (int i = 0; i < C::COLS_WARP; ++i)
+                            if (col0 + i < args.rows_b)
+                                d[static_cast<int64_t>(col0 + i) * args.ldo] =
+                                    __float2bfloat16_rn(__uint_as_float(v[i]) * args.alpha);
                     } else {
-                        float *d = static_cast<float *>(args.out);
+                        float *d = static_cast<float *>(args.out) + ra;
 #pragma unroll
-                        for (int i = 0; i < CH; ++i) {
-                            const int rb = row_b0 + c * CH + i;
-                            if (rb < args.rows_b) d[static_cast<int64_t>(rb) * args.ldo + ra] = __uint_as_float(v[i]) * args.alpha;
-                        }
+                        for (int i = 0; i < C::COLS_WARP; ++i)
+                            if (col0 + i < args.rows_b)
+                                d[static_cast<int64_t>(col0 + i) * args.ldo] = __uint_as_float(v[i]) * args.alpha;
                     }
                 }
             }
@@ -452,14 +463,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 acc_phase ^= 1u;
             }
         }
-        if (leader) bulk_wait_group<0>();
+        if (lane == 0) bulk_wait_group<0>();
     }
 
     __syncwarp();
     tc_fence_before();
-    __syncthreads();
+    if constexpr (CG == 2) cluster_sync(); else __syncthreads();
     tc_fence_after();
-    if (warp == 1) tmem_dealloc(tmem, C::TMEM_COLS);
+    if (warp == 1) tmem_dealloc<CG>(tmem, C::TMEM_COLS);
 }
 
 // Split-K: D[rb][ra] = alpha * sum_s ws[s][rb][ra] (fixed order, deterministic).
@@ -482,27 +493,39 @@ __global__ void splitk_reduce_kernel(const float *__restrict__ ws, void *__restr
 }
 
 // Scale reorder: row-major sf[rows][ksf] -> 128x4 atoms. One thread writes one
-// 4-byte word of the output: word w of atom (rb, cb) holds row
-// rb*128 + 32*(w%4) + (w/4)%32, columns 4cb..4cb+3 (zero past the matrix).
-__global__ void scale_reorder_kernel(const uint8_t *__restrict__ sf, uint32_t *__restrict__ out, int64_t rows,
-                                     int64_t ksf, int64_t kc4, int64_t words)
+// 16-byte line of an atom: line i of atom (rb, cb) holds rows rb*128 + i + 32j
+// (j = 0..3), columns 4cb..4cb+3 (zero past the matrix). A block of 256 threads
+// covers 8 consecutive atoms of one 128-row block, so its reads of a row fall
+// in one or two 32-byte sectors.
+__global__ void scale_reorder_kernel(const uint8_t *__restrict__ sf, uint4 *__restrict__ out, int64_t rows,
+                                     int64_t ksf, int64_t kc4, int64_t lines)
 {
-    for (int64_t w = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; w < words;
-         w += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        const int64_t atom = w >> 7;
-        const int within = static_cast<int>(w & 127);
-        const int i = within >> 2, j = within & 3;
+    // 32-bit loads only when every row's 4-column group is 4-byte aligned
+    const bool words = (ksf & 3) == 0 && (reinterpret_cast<uintptr_t>(sf) & 3) == 0;
+    for (int64_t l = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; l < lines;
+         l += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t atom = l >> 5;
+        const int i = static_cast<int>(l & 31);
         const int64_t rb = atom / kc4, cb = atom - rb * kc4;
-        const int64_t r = rb * 128 + 32 * j + i;
         const int64_t c0 = cb * 4;
-        uint32_t word = 0;
-        if (r < rows) {
-            const uint8_t *row = sf + r * ksf;
+        uint32_t w[4];
 #pragma unroll
-            for (int t = 0; t < 4; ++t)
-                if (c0 + t < ksf) word |= static_cast<uint32_t>(row[c0 + t]) << (8 * t);
+        for (int j = 0; j < 4; ++j) {
+            const int64_t r = rb * 128 + 32 * j + i;
+            uint32_t word = 0;
+            if (r < rows) {
+                const uint8_t *row = sf + r * ksf;
+                if (words) {
+                    word = __ldg(reinterpret_cast<const uint32_t *>(row + c0));
+                } else {
+#pragma unroll
+                    for (int t = 0; t < 4; ++t)
+                        if (c0 + t < ksf) word |= static_cast<uint32_t>(__ldg(row + c0 + t)) << (8 * t);
+                }
+            }
+            w[j] = word;
         }
-        out[w] = word;
+        out[l] = make_uint4(w[0], w[1], w[2], w[3]);
     }
 }
 
@@ -514,11 +537,14 @@ std::mutex g_mu;
 int64_t g_wait_ms = -1;
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
+constexpr int kNumKernels = 14;   // (CTA group 1: five widths + group 2: two widths) x two formats
+
 struct DeviceInfo {
     bool probed = false;
     bool ok = false;
     int sms = 0;
-    bool attr_set[9] = {};
+    bool attr_set[kNumKernels] = {};
+    int max_clusters[kNumKernels] = {};
 };
 DeviceInfo g_dev[64];
 
@@ -562,15 +588,14 @@ fp4_status device_info(int &dev, DeviceInfo *&info)
 }
 
 bool encode_2d(CUtensorMap *m, CUtensorMapDataType dt, const void *ptr, uint64_t inner, uint64_t outer,
-               uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer)
+               uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw)
 {
     const cuuint64_t dims[2] = {inner, outer};
     const cuuint64_t strides[1] = {row_bytes};
     const cuuint32_t box[2] = {box_inner, box_outer};
     const cuuint32_t estr[2] = {1, 1};
-    return g_encode(m, dt, 2, const_cast<void *>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    return g_encode(m, dt, 2, const_cast<void *>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -588,39 +613,97 @@ int bn_index(int bn)
     }
 }
 
-template <int BN>
-cudaError_t launch_gemm(DeviceInfo &info, int grid, const CUtensorMap &ta, const CUtensorMap &tb,
-                        const CUtensorMap &td, const Args &args, cudaStream_t stream)
+struct Maps {
+    CUtensorMap a, b, sfa, sfb, d;
+};
+
+template <int CG, int BN, bool MX>
+cudaError_t launch_gemm(DeviceInfo &info, int kidx, int units, int cap, const Maps &m, const Args &args,
+                        cudaStream_t stream)
 {
-    using C = Cfg<BN>;
-    const int idx = bn_index(BN);
-    if (!info.attr_set[idx]) {
-        cudaError_t e = cudaFuncSetAttribute(fp4_gemm_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             C::SMEM_BYTES);
+    using C = Cfg<CG, BN, MX>;
+    auto kern = fp4_gemm_kernel<CG, BN, MX>;
+    cudaLaunchAttribute cluster_attr[1];
+    cluster_attr[0].id = cudaLaunchAttributeClusterDimension;
+    cluster_attr[0].val.clusterDim.x = CG;
+    cluster_attr[0].val.clusterDim.y = 1;
+    cluster_attr[0].val.clusterDim.z = 1;
+    if (!info.attr_set[kidx]) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
         if (e != cudaSuccess) return e;
-        info.attr_set[idx] = true;
+        int slots = info.sms;
+        if (CG == 2) {
+            cudaLaunchConfig_t qc = {};
+            qc.gridDim = dim3(2 * info.sms, 1, 1);
+            qc.blockDim = dim3(kThreads, 1, 1);
+            qc.dynamicSmemBytes = C::SMEM_BYTES;
+            qc.attrs = cluster_attr;
+            qc.numAttrs = 1;
+            int n = 0;
+            if (cudaOccupancyMaxActiveClusters(&n, kern, &qc) != cudaSuccess || n <= 0) {
+                cudaGetLastError();
+                n = info.sms / 2;
+            }
+            slots = n;
+        }
+        info.max_clusters[kidx] = slots;
+        info.attr_set[kidx] = true;
     }
-    fp4_gemm_kernel<BN><<<grid, kThreads, C::SMEM_BYTES, stream>>>(ta, tb, td, args);
-    return cudaGetLastError();
+    const int slots = info.max_clusters[kidx];
+    int groups = std::min(units, slots);
+    if (cap > 0) groups = std::min(groups, std::max(1, cap / CG));
+    groups = std::max(groups, 1);
+    cudaLaunchConfig_t lc = {};
+    lc.gridDim = dim3(groups * CG, 1, 1);
+    lc.blockDim = dim3(kThreads, 1, 1);
+    lc.dynamicSmemBytes = C::SMEM_BYTES;
+    lc.stream = stream;
+    if (CG == 2) {
+        lc.attrs = cluster_attr;
+        lc.numAttrs = 1;
+    }
+    return cudaLaunchKernelEx(&lc, kern, m.a, m.b, m.sfa, m.sfb, m.d, args);
 }
 
-cudaError_t launch_by_bn(int bn, DeviceInfo &info, int grid, const CUtensorMap &ta, const CUtensorMap &tb,
-                         const CUtensorMap &td, const Args &args, cudaStream_t stream)
+cudaError_t launch_by_cfg(int cg, int bn, bool mx, DeviceInfo &info, int units, int cap, const Maps &m,
+                          const Args &args, cudaStream_t stream)
 {
-    switch (bn) {
-    case 16: return launch_gemm<16>(info, grid, ta, tb, td, args, stream);
-    case 32: return launch_gemm<32>(info, grid, ta, tb, td, args, stream);
-    case 64: return launch_gemm<64>(info, grid, ta, tb, td, args, stream);
-    case 128: return launch_gemm<128>(info, grid, ta, tb, td, args, stream);
-    default: return launch_gemm<256>(info, grid, ta, tb, td, args, stream);
+    const int k = (cg == 2 ? 10 + (bn == 256 ? 2 : 0) : bn_index(bn) * 2) + (mx ? 1 : 0);
+#define FP4_LAUNCH(CG_, BN_, MX_) return launch_gemm<CG_, BN_, MX_>(info, k, units, cap, m, args, stream)
+    if (cg == 2) {
+        if (bn == 256) {
+            if (mx) FP4_LAUNCH(2, 256, true);
+            FP4_LAUNCH(2, 256, false);
+        }
+        if (mx) FP4_LAUNCH(2, 128, true);
+        FP4_LAUNCH(2, 128, false);
     }
+    switch (bn) {
+    case 16:
+        if (mx) FP4_LAUNCH(1, 16, true);
+        FP4_LAUNCH(1, 16, false);
+    case 32:
+        if (mx) FP4_LAUNCH(1, 32, true);
+        FP4_LAUNCH(1, 32, false);
+    case 64:
+        if (mx) FP4_LAUNCH(1, 64, true);
+        FP4_LAUNCH(1, 64, false);
+    case 128:
+        if (mx) FP4_LAUNCH(1, 128, true);
+        FP4_LAUNCH(1, 128, false);
+    default:
+        if (mx) FP4_LAUNCH(1, 256, true);
+        FP4_LAUNCH(1, 256, false);
+    }
+#undef FP4_LAUNCH
 }
 
 struct Plan {
     bool swap;
     int bn;
+    int cg;
     int splits;
-    int grid;
+    int cap;
 };
 
 int pow2_bn(int64_t rows)
@@ -632,8 +715,8 @@ int pow2_bn(int64_t rows)
     return 256;
 }
 
-// Chooses direct vs swap-AB, the tile N and the K split. `tma_ok` says whether
-// D can take TMA stores (row pitch and base 16-byte aligned).
+// Chooses direct vs swap-AB, the tile N, the CTA group and the K split.
+// `tma_ok` says whether D's rows can take TMA stores (pitch 16-byte aligned).
 fp4_status make_plan(int64_t M, int64_t N, int64_t K, bool tma_ok, int sms, const fp4_gemm_config *cfg, Plan &p)
 {
     const int mode = cfg ? cfg->mode : 0;
@@ -647,23 +730,28 @@ fp4_status make_plan(int64_t M, int64_t N, int64_t K, bool tma_ok, int sms, cons
     if (!p.swap && !tma_ok) return FP4_ERR_MISALIGNED;
     const int64_t rows_b = p.swap ? M : N;
     const int64_t rows_a = p.swap ? N : M;
-    int bn = (cfg && cfg->bn) ? cfg->bn : (p.swap ? pow2_bn(rows_b) : 256);
+    const int bn = (cfg && cfg->bn) ? cfg->bn : (p.swap ? pow2_bn(rows_b) : 256);
     if (bn_index(bn) < 0) return FP4_ERR_INVALID_ARG;
-    if (!p.swap && bn < 128) return FP4_ERR_UNSUPPORTED;           // direct mode stages through TMA store tiles
+    if (!p.swap && bn < 128) return FP4_ERR_UNSUPPORTED;           // direct mode stores 64-column warp boxes
     if (rows_b > bn && bn < 128) return FP4_ERR_UNSUPPORTED;       // N-side tiles must start on scale blocks
     p.bn = bn;
-    const int64_t tiles = cdiv(rows_a, kBM) * cdiv(rows_b, bn);
+    const int cg = (cfg && cfg->cta_group) ? cfg->cta_group : ((bn >= 128 && rows_a > 128) ? 2 : 1);
+    if (cg != 1 && cg != 2) return FP4_ERR_INVALID_ARG;
+    if (cg == 2 && bn < 128) return FP4_ERR_UNSUPPORTED;
+    p.cg = cg;
+    const int64_t tiles = cdiv(rows_a, kBM * cg) * cdiv(rows_b, bn);
     const int64_t k_tiles = cdiv(K, kBK);
+    const int slots = std::max(1, sms / cg);
     int splits = (cfg && cfg->splits) ? cfg->splits : 0;
     if (splits < 0) return FP4_ERR_INVALID_ARG;
-    if (splits > 1 && !p.swap) return FP4_ERR_UNSUPPORTED;
+    if (splits > 1 && !p.swap) return FP4_ERR_UNSUPPORTED;         // partials are written swap-AB style
     if (splits == 0) {
         splits = 1;
-        if (p.swap && tiles < sms) {
+        if (p.swap && tiles < slots) {
             // minimise (waves x k-tiles per split), preferring fewer splits on ties
             double best = 1e30;
             for (int s = 1; s <= std::min<int64_t>(k_tiles, 16); ++s) {
-                const double waves = static_cast<double>(cdiv(tiles * s, sms));
+                const double waves = static_cast<double>(cdiv(tiles * s, slots));
                 const double cost = waves * static_cast<double>(cdiv(k_tiles, s)) * (1.0 + 0.02 * (s - 1));
                 if (cost < best - 1e-9) {
                     best = cost;
@@ -672,23 +760,21 @@ fp4_status make_plan(int64_t M, int64_t N, int64_t K, bool tma_ok, int sms, cons
             }
         }
     }
-    splits = static_cast<int>(std::min<int64_t>(splits, k_tiles));
-    p.splits = std::max(1, splits);
-    const int64_t units = tiles * p.splits;
-    int cap = (cfg && cfg->max_ctas > 0) ? cfg->max_ctas : sms;
-    p.grid = static_cast<int>(std::min<int64_t>(units, cap));
+    p.splits = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(splits, k_tiles)));
+    p.cap = (cfg && cfg->max_ctas > 0) ? cfg->max_ctas : 0;
     return FP4_OK;
 }
 
-fp4_status reorder_launch(const void *sf_plain, void *sf_atom, int64_t rows, int64_t ksf, cudaStream_t stream)
+fp4_status reorder_launch(const void *sf_plain, void *sf_atom, int64_t rows, int64_t ksf, int sms,
+                          cudaStream_t stream)
 {
     const int64_t kc4 = cdiv(ksf, 4);
-    const int64_t words = cdiv(rows, 128) * kc4 * 128;
-    if (words == 0) return FP4_OK;
+    const int64_t lines = cdiv(rows, 128) * kc4 * 32;
+    if (lines == 0) return FP4_OK;
     const int threads = 256;
-    const int64_t blocks = std::min<int64_t>(cdiv(words, threads), 148 * 16);
+    const int64_t blocks = std::min<int64_t>(cdiv(lines, threads), static_cast<int64_t>(sms) * 32);
     scale_reorder_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
-        static_cast<const uint8_t *>(sf_plain), static_cast<uint32_t *>(sf_atom), rows, ksf, kc4, words);
+        static_cast<const uint8_t *>(sf_plain), static_cast<uint4 *>(sf_atom), rows, ksf, kc4, lines);
     return cudaGetLastError() == cudaSuccess ? FP4_OK : FP4_ERR_CUDA;
 }
 
@@ -719,7 +805,8 @@ fp4_status gemm_impl(fp4_format fmt, int prepacked, const void *A, const void *s
     fp4_status st = device_info(dev, info);
     if (st != FP4_OK) return st;
 
-    const int vec = fmt == FP4_FMT_NVFP4 ? 16 : 32;
+    const bool mx = fmt == FP4_FMT_MXFP4;
+    const int vec = mx ? 32 : 16;
     const int64_t ksf = K / vec;
     const int64_t kc4 = cdiv(ksf, 4);
     const bool tma_ok = (N * esize) % 16 == 0;
@@ -732,8 +819,9 @@ fp4_status gemm_impl(fp4_format fmt, int prepacked, const void *A, const void *s
     const void *sf_a = plan.swap ? sfB : sfA, *sf_b = plan.swap ? sfA : sfB;
 
     // scratch: reordered scales and split-K partials (stream-ordered)
-    const size_t atoms_a = static_cast<size_t>(cdiv(rows_a, 128) * kc4 * kAtomBytes);
-    const size_t atoms_b = static_cast<size_t>(cdiv(rows_b, 128) * kc4 * kAtomBytes);
+    const int64_t rb_a = cdiv(rows_a, 128), rb_b = cdiv(rows_b, 128);
+    const size_t atoms_a = static_cast<size_t>(rb_a * kc4 * kAtomBytes);
+    const size_t atoms_b = static_cast<size_t>(rb_b * kc4 * kAtomBytes);
     const size_t ws_bytes = plan.splits > 1 ? static_cast<size_t>(plan.splits) * rows_a * rows_b * 4 : 0;
     const size_t scratch_bytes = (prepacked ? 0 : atoms_a + atoms_b) + ws_bytes;
     uint8_t *scratch = nullptr;
@@ -747,47 +835,54 @@ fp4_status gemm_impl(fp4_format fmt, int prepacked, const void *A, const void *s
         const uint8_t *sfb_atoms = static_cast<const uint8_t *>(sf_b);
         uint8_t *ws = scratch + (prepacked ? 0 : atoms_a + atoms_b);
         if (!prepacked) {
-            if ((result = reorder_launch(sf_a, scratch, rows_a, ksf, stream)) != FP4_OK) break;
-            if ((result = reorder_launch(sf_b, scratch + atoms_a, rows_b, ksf, stream)) != FP4_OK) break;
+            if ((result = reorder_launch(sf_a, scratch, rows_a, ksf, info->sms, stream)) != FP4_OK) break;
+            if ((result = reorder_launch(sf_b, scratch + atoms_a, rows_b, ksf, info->sms, stream)) != FP4_OK) break;
             sfa_atoms = scratch;
             sfb_atoms = scratch + atoms_a;
         }
-        CUtensorMap tmap_a, tmap_b, tmap_d;
-        std::memset(&tmap_d, 0, sizeof tmap_d);
-        if (!encode_2d(&tmap_a, CU_TENSOR_MAP_DATA_TYPE_UINT8, op_a, static_cast<uint64_t>(K / 2),
-                       static_cast<uint64_t>(rows_a), static_cast<uint64_t>(K / 2), kBKBytes, kBM) ||
-            !encode_2d(&tmap_b, CU_TENSOR_MAP_DATA_TYPE_UINT8, op_b, static_cast<uint64_t>(K / 2),
+        const int apk = mx ? 2 : 4;
+        const int nrb = static_cast<int>(cdiv(plan.bn, 128));
+        Maps m;
+        std::memset(&m, 0, sizeof m);
+        // Scale atoms are viewed as int64 rows of ceil(K/vec/4) * 64 elements per
+        // 128-row block; one box is one k-tile's atoms of 1 (slot A) or
+        // ceil(BN/128) (slot B) blocks, zero-filled past the matrix.
+        if (!encode_2d(&m.a, CU_TENSOR_MAP_DATA_TYPE_UINT8, op_a, static_cast<uint64_t>(K / 2),
+                       static_cast<uint64_t>(rows_a), static_cast<uint64_t>(K / 2), kBKBytes, kBM,
+                       CU_TENSOR_MAP_SWIZZLE_128B) ||
+            !encode_2d(&m.b, CU_TENSOR_MAP_DATA_TYPE_UINT8, op_b, static_cast<uint64_t>(K / 2),
                        static_cast<uint64_t>(rows_b), static_cast<uint64_t>(K / 2), kBKBytes,
-                       static_cast<uint32_t>(plan.bn))) {
+                       static_cast<uint32_t>(plan.bn / plan.cg), CU_TENSOR_MAP_SWIZZLE_128B) ||
+            !encode_2d(&m.sfa, CU_TENSOR_MAP_DATA_TYPE_INT64, sfa_atoms, static_cast<uint64_t>(kc4 * 64),
+                       static_cast<uint64_t>(rb_a), static_cast<uint64_t>(kc4 * kAtomBytes),
+                       static_cast<uint32_t>(apk * 64), 1, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+            !encode_2d(&m.sfb, CU_TENSOR_MAP_DATA_TYPE_INT64, sfb_atoms, static_cast<uint64_t>(kc4 * 64),
+                       static_cast<uint64_t>(rb_b), static_cast<uint64_t>(kc4 * kAtomBytes),
+                       static_cast<uint32_t>(apk * 64), static_cast<uint32_t>(nrb), CU_TENSOR_MAP_SWIZZLE_NONE)) {
             result = FP4_ERR_CUDA;
             break;
         }
         Args a;
         std::memset(&a, 0, sizeof a);
-        a.sfa = sfa_atoms;
-        a.sfb = sfb_atoms;
         a.wait_ns = wait_limit_ns();
         a.rows_a = static_cast<int32_t>(rows_a);
         a.rows_b = static_cast<int32_t>(rows_b);
-        a.K = static_cast<int32_t>(K);
-        a.kc4 = static_cast<int32_t>(kc4);
         a.k_tiles = static_cast<int32_t>(cdiv(K, kBK));
-        a.splits = plan.splits;
         a.kps = static_cast<int32_t>(cdiv(a.k_tiles, plan.splits));
         a.splits = static_cast<int32_t>(cdiv(a.k_tiles, a.kps));   // no empty split
-        a.tiles_a = static_cast<int32_t>(cdiv(rows_a, kBM));
+        a.tiles_a = static_cast<int32_t>(cdiv(rows_a, kBM * plan.cg));
         a.tiles_b = static_cast<int32_t>(cdiv(rows_b, plan.bn));
         a.units = a.tiles_a * a.tiles_b * a.splits;
         a.group_b = std::max(1, std::min(a.tiles_b, 8));
-        a.mx = fmt == FP4_FMT_MXFP4;
         a.bf16 = out == FP4_OUT_BF16;
         a.alpha = alpha;
         if (!plan.swap) {
             a.mode = kEpiTmaStore;
             a.out = D;
             const CUtensorMapDataType dt = a.bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
-            if (!encode_2d(&tmap_d, dt, D, static_cast<uint64_t>(N), static_cast<uint64_t>(M),
-                           static_cast<uint64_t>(N * esize), static_cast<uint32_t>(128 / esize), kBM)) {
+            if (!encode_2d(&m.d, dt, D, static_cast<uint64_t>(N), static_cast<uint64_t>(M),
+                           static_cast<uint64_t>(N * esize), static_cast<uint32_t>(128 / esize), 32,
+                           CU_TENSOR_MAP_SWIZZLE_128B)) {
                 result = FP4_ERR_CUDA;
                 break;
             }
@@ -801,8 +896,7 @@ fp4_status gemm_impl(fp4_format fmt, int prepacked, const void *A, const void *s
             a.out = D;
             a.ldo = N;
         }
-        const int grid = std::min(plan.grid, a.units);
-        if (launch_by_bn(plan.bn, *info, grid, tmap_a, tmap_b, tmap_d, a, stream) != cudaSuccess) {
+        if (launch_by_cfg(plan.cg, plan.bn, mx, *info, a.units, plan.cap, m, a, stream) != cudaSuccess) {
             result = FP4_ERR_CUDA;
             break;
         }
@@ -911,7 +1005,7 @@ fp4_status fp4_scale_reorder(const void *sf_plain, void *sf_atom, int64_t rows, 
     DeviceInfo *info;
     fp4_status st = device_info(dev, info);
     if (st != FP4_OK) return st;
-    return reorder_launch(sf_plain, sf_atom, rows, k / vec, stream);
+    return reorder_launch(sf_plain, sf_atom, rows, k / vec, info->sms, stream);
 }
 
 fp4_status fp4_get_device_status(cudaStream_t stream)

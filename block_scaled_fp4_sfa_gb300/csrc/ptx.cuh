@@ -100,15 +100,25 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map)
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
-// 2-D tiled TMA load into shared memory, completing `bytes` on the mbarrier.
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, uint32_t bar,
-                                            int32_t x, int32_t y)
+// 2-D tiled TMA load into this CTA's shared memory, completing its bytes on the
+// mbarrier. CG = 2 (tcgen05 CTA pair): the mbarrier may be the peer CTA's.
+template <int CG>
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, uint32_t bar, int32_t x,
+                                            int32_t y)
 {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
-        : "memory");
+    if constexpr (CG == 2) {
+        asm volatile(
+            "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+            " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+            "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
+            : "memory");
+    } else {
+        asm volatile(
+            "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+            " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+            "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
+            : "memory");
+    }
 }
 
 // Same, with an L2 eviction-priority hint (a createpolicy value).
@@ -175,22 +185,34 @@ __device__ __forceinline__ void bulk_wait_group()
 
 // ---- tcgen05: tensor memory ------------------------------------------------------
 
+// TMEM allocation. With CG = 2 one warp of each CTA of the pair issues it.
+template <int CG>
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols)
 {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
-                 "r"(ncols)
-                 : "memory");
+    if constexpr (CG == 2)
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
+                     : "memory");
+    else
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
+                     : "memory");
 }
 
+template <int CG>
 __device__ __forceinline__ void tmem_relinquish()
 {
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    if constexpr (CG == 2)
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+    else
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
 }
 
+template <int CG>
 __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols)
 {
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
-                 : "memory");
+    if constexpr (CG == 2)
+        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+    else
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
 }
 
 __device__ __forceinline__ void tc_fence_before()
@@ -204,47 +226,61 @@ __device__ __forceinline__ void tc_fence_after()
 }
 
 // Arrive once on `bar` when every tcgen05 async operation issued so far by this
-// thread has completed.
-__device__ __forceinline__ void tc_commit(uint32_t bar)
+// thread has completed. CG = 2: the arrive goes to the barrier at the same
+// offset in each CTA of the pair named in `mask` (default both).
+template <int CG>
+__device__ __forceinline__ void tc_commit(uint32_t bar, uint16_t mask = 3)
 {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-                 : "memory");
+    if constexpr (CG == 2)
+        asm volatile(
+            "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+                bar),
+            "h"(mask)
+            : "memory");
+    else
+        asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                     : "memory");
 }
 
 // Copy one 32-row x 16-byte shared-memory matrix into 4 TMEM columns, repeated
-// in all four 32-lane sub-partitions (the block-scale factor placement).
+// in all four 32-lane sub-partitions (the block-scale factor placement). CG = 2:
+// done in both CTAs of the pair, each from its own shared memory.
+template <int CG>
 __device__ __forceinline__ void tc_cp_32x128b_warpx4(uint32_t taddr, uint64_t sdesc)
 {
-    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+    if constexpr (CG == 2)
+        asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+    else
+        asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
 }
 
-// Block-scaled FP4 MMA, 16-element scale blocks (UE4M3 scales):
-//   D[tmem] (+)= A[smem] x B[smem]^T, K = 64.
-__device__ __forceinline__ void tc_mma_fp4_vec16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
-                                                 uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
-                                                 uint32_t accumulate)
+// Block-scaled FP4 MMA, D[tmem] (+)= A[smem] x B[smem]^T with K = 64:
+// MX = false: 16-element scale blocks, UE4M3 scales (scale_vec::4X);
+// MX = true:  32-element scale blocks, UE8M0 scales (scale_vec::2X).
+template <int CG, bool MX>
+__device__ __forceinline__ void tc_mma_fp4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                           uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate)
 {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %6, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n\t"
-        "}" ::"r"(d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
-        : "memory");
+#define FP4_MMA_ASM(GROUP, VEC)                                                                                  \
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"                                            \
+                 "tcgen05.mma.cta_group::" GROUP ".kind::mxf4nvf4.block_scale.scale_vec::" VEC                  \
+                 " [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),                                          \
+                 "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)               \
+                 : "memory")
+    if constexpr (CG == 2) {
+        if constexpr (MX) FP4_MMA_ASM("2", "2X"); else FP4_MMA_ASM("2", "4X");
+    } else {
+        if constexpr (MX) FP4_MMA_ASM("1", "2X"); else FP4_MMA_ASM("1", "4X");
+    }
+#undef FP4_MMA_ASM
 }
 
-// Block-scaled FP4 MMA, 32-element scale blocks (UE8M0 scales), K = 64.
-__device__ __forceinline__ void tc_mma_fp4_vec32(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
-                                                 uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
-                                                 uint32_t accumulate)
+// 32 lanes x 8 columns of 32-bit TMEM -> 8 registers per thread.
+__device__ __forceinline__ void tmem_ld_32x32b_x8(uint32_t taddr, uint32_t (&r)[8])
 {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %6, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], [%5], p;\n\t"
-        "}" ::"r"(d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
-        : "memory");
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+                 : "r"(taddr));
 }
 
 // 32 lanes x 32 columns of 32-bit TMEM -> 32 registers per thread (thread i gets lane i).
@@ -279,6 +315,35 @@ __device__ __forceinline__ void tmem_ld_wait()
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// ---- clusters ------------------------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t cluster_ctarank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// Shared::cluster address of `addr` (a shared address of this CTA) in CTA `rank`.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank)
+{
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+
+// Arrive on an mbarrier given by a shared::cluster address (possibly another CTA's).
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr)
+{
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
+// Every thread of every CTA of the cluster.
+__device__ __forceinline__ void cluster_sync()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 // ---- descriptors ---------------------------------------------------------------------
 
 // tcgen05 shared-memory matrix descriptor: start address, leading/stride byte
@@ -300,7 +365,7 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo_bytes
 // operands E2M1 (format code 1), K-major, dense, no negation:
 //   bits 4-5 B scale-factor byte id, 7-9 A format, 10-12 B format, 17-22 N>>3,
 //   23 scale type (0 UE4M3, 1 UE8M0), 27-28 M>>7, 29-30 A scale-factor byte id.
-__host__ __device__ __forceinline__ uint32_t idesc_fp4(uint32_t m, uint32_t n, bool ue8m0,
+__host__ __device__ constexpr uint32_t idesc_fp4(uint32_t m, uint32_t n, bool ue8m0,
                                                         uint32_t a_sf_id, uint32_t b_sf_id)
 {
     uint32_t d = 0;

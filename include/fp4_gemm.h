@@ -70,19 +70,22 @@ typedef enum { FP4_OUT_F32 = 0, FP4_OUT_BF16 = 1 } fp4_out_dtype;
 typedef enum { FP4_FMT_NVFP4 = 0, FP4_FMT_MXFP4 = 1 } fp4_format;
 
 /* Optional overrides of the launch plan (zero-initialise for "automatic").
- *   mode:     0 auto; 1 direct (A on the 128-row MMA side, D written by TMA
- *             store); 2 swap-AB (B on the 128-row side, D^T tiles written with
- *             coalesced stores; the trick of "Hopper GEMM in CUTLASS C++ and
- *             the CuTe DSL, part 1", section on the swapped operands).
- *   bn:       0 auto; else the MMA N of a tile: 16, 32, 64, 128 or 256.
- *             Several tiles along the N side need bn 128 or 256.
- *   splits:   0 auto; else the number of K splits (swap-AB mode only).
- *   max_ctas: 0 = one persistent CTA per SM; else a cap on the grid.         */
+ *   mode:      0 auto; 1 direct (A on the MMA's M side, D written by TMA
+ *              stores); 2 swap-AB (B on the M side, D^T tiles written with
+ *              coalesced stores; the trick of "Hopper GEMM in CUTLASS C++ and
+ *              the CuTe DSL, part 1", section on the swapped operands).
+ *   bn:        0 auto; else the MMA N of a tile: 16, 32, 64, 128 or 256.
+ *              Direct mode needs 128 or 256; so do several tiles on the N side.
+ *   splits:    0 auto; else the number of K splits (swap-AB mode only).
+ *   max_ctas:  0 = as many persistent CTAs as fit (one per SM); else a cap.
+ *   cta_group: 0 auto; 1 = one CTA per 128-row MMA; 2 = a CTA pair (cluster
+ *              of 2) per 256-row MMA (bn 128 or 256).                        */
 typedef struct {
     int32_t mode;
     int32_t bn;
     int32_t splits;
     int32_t max_ctas;
+    int32_t cta_group;
 } fp4_gemm_config;
 
 /* NVFP4 GEMM (E4M3 scales, one per 16 K-elements), plain row-major scales. */

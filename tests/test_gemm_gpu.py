@@ -124,6 +124,18 @@ def test_scale_reorder_bit_exact(fp4, orc, rows, K, vec):
     np.testing.assert_array_equal(out.cpu().numpy(), orc.scale_reorder(sf, rows, K // vec))
 
 
+def test_scale_reorder_unaligned_source(fp4, orc):
+    # plain scales need no alignment: an odd source address takes the byte path
+    rows, K, vec = 200, 1024, 16
+    sf = np.random.default_rng(1).integers(0, 256, (rows, K // vec)).astype(np.uint8)
+    buf = torch.zeros(sf.size + 16, dtype=torch.uint8, device="cuda")
+    buf[1:1 + sf.size] = _dev(sf.ravel())
+    out = torch.empty(fp4.scale_atom_bytes(rows, K, vec), dtype=torch.uint8, device="cuda")
+    fp4.scale_reorder(buf.data_ptr() + 1, out, rows, K, vec)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(out.cpu().numpy(), orc.scale_reorder(sf, rows, K // vec))
+
+
 # ---- small problems, full comparison -------------------------------------------------------
 
 def test_smallest_config_matches(fp4, orc):
@@ -156,9 +168,14 @@ def test_one_hot_products_exact(fp4, orc, fmt):
     sfB = rng.integers(lo, hi, (N, K // vec)).astype(np.uint8)
     inp = W.GemmInputs(fmt, M, N, K, W.pack_codes(codes_a), sfA, W.pack_codes(codes_b), sfB, 1.0, "f32", "onehot")
     ref, _ = orc.gemm_rows(inp)
-    for cfg in (None, fp4.GemmConfig(mode=2, bn=256)):
+    plans = [None,
+             fp4.GemmConfig(mode=1, bn=256, cta_group=1), fp4.GemmConfig(mode=1, bn=128, cta_group=1),
+             fp4.GemmConfig(mode=1, bn=256, cta_group=2), fp4.GemmConfig(mode=1, bn=128, cta_group=2),
+             fp4.GemmConfig(mode=2, bn=256, cta_group=1), fp4.GemmConfig(mode=2, bn=256, cta_group=2)]
+    for cfg in plans:
         got = run(fp4, inp, cfg)
-        np.testing.assert_array_equal(got, ref)
+        what = "auto" if cfg is None else (cfg.mode, cfg.bn, cfg.cta_group)
+        np.testing.assert_array_equal(got, ref, err_msg=str(what))
 
 
 @pytest.mark.parametrize("fmt", ["nvfp4", "mxfp4"])
@@ -169,8 +186,10 @@ def test_uniform_codes_several_tiles(fp4, orc, fmt, out):
 
 
 PLAN_CASES = [
-    # (mode, bn, splits): direct with both tile widths, swap-AB with every width, split-K
-    (1, 256, 0), (1, 128, 0), (2, 256, 0), (2, 128, 0), (2, 256, 3), (2, 128, 2),
+    # (mode, bn, splits, cta_group): direct and swap-AB, both tile widths, one CTA
+    # or a CTA pair per MMA, split-K
+    (1, 256, 0, 1), (1, 128, 0, 1), (1, 256, 0, 2), (1, 128, 0, 2), (2, 256, 0, 1), (2, 128, 0, 1),
+    (2, 256, 0, 2), (2, 128, 2, 2), (2, 256, 3, 1), (2, 128, 2, 1), (2, 256, 3, 2), (1, 256, 0, 2),
 ]
 
 
@@ -187,7 +206,7 @@ def test_fuzz_small_shapes(fp4, orc, seed):
     dist = "t3" if seed % 3 == 0 else "normal"
     inp = W.make_random(fmt, M, N, K, dist=dist, alpha=float(rng.choice([1.0, 0.5, 3.0])), out=out, seed=seed)
     check_full(orc, inp, run(fp4, inp), "auto plan")
-    mode, bn, splits = PLAN_CASES[seed % len(PLAN_CASES)]
+    mode, bn, splits, cg = PLAN_CASES[seed % len(PLAN_CASES)]
     esize = 4 if out == "f32" else 2
     rows_b = N if mode == 1 else M
     if mode == 1 and (N * esize) % 16:
@@ -195,8 +214,8 @@ def test_fuzz_small_shapes(fp4, orc, seed):
         rows_b = M
     if rows_b > bn and bn < 128:
         bn = 256
-    cfg = fp4.GemmConfig(mode=mode, bn=bn, splits=splits)
-    check_full(orc, inp, run(fp4, inp, cfg), "plan %s" % ((mode, bn, splits),))
+    cfg = fp4.GemmConfig(mode=mode, bn=bn, splits=splits, cta_group=cg)
+    check_full(orc, inp, run(fp4, inp, cfg), "plan %s" % ((mode, bn, splits, cg),))
 
 
 @pytest.mark.parametrize("M", [1, 7, 16, 33, 64, 100, 128, 200, 256])
@@ -212,6 +231,8 @@ def test_k_tail_not_multiple_of_tile(fp4, orc):
             inp = W.make_random(fmt, 130, 136, K, out="f32", seed=K)
             check_full(orc, inp, run(fp4, inp), "K=%d %s" % (K, fmt))
             check_full(orc, inp, run(fp4, inp, fp4.GemmConfig(mode=2, bn=256)), "K=%d %s swap" % (K, fmt))
+            check_full(orc, inp, run(fp4, inp, fp4.GemmConfig(mode=1, bn=128, cta_group=2)),
+                       "K=%d %s pair" % (K, fmt))
 
 
 def test_prepacked_equals_plain(fp4, orc):
@@ -235,7 +256,9 @@ def test_persistent_grid_cap(fp4, orc):
     # few CTAs, many tiles each: exercises the stage / accumulator phase wrap-around
     inp = W.make_random("nvfp4", 1024, 1024, 1024, out="f32", seed=6)
     for cfg in (fp4.GemmConfig(max_ctas=3), fp4.GemmConfig(mode=2, bn=128, max_ctas=2),
-                fp4.GemmConfig(mode=1, bn=128, max_ctas=1)):
+                fp4.GemmConfig(mode=1, bn=128, max_ctas=1, cta_group=1),
+                fp4.GemmConfig(mode=1, bn=256, max_ctas=2, cta_group=2),
+                fp4.GemmConfig(mode=2, bn=128, max_ctas=4, cta_group=2, splits=3)):
         check_full(orc, inp, run(fp4, inp, cfg), "cap")
 
 
@@ -286,4 +309,6 @@ def test_error_statuses_launch_nothing(fp4):
     assert g("nvfp4", z, z, z, z, 1.0, D, 64, 64, 64, "f32", config=fp4.GemmConfig(mode=1, bn=64)) == 2
     assert g("nvfp4", z, z, z, z, 1.0, D, 64, 64, 64, "f32", config=fp4.GemmConfig(mode=1, splits=2)) == 2
     assert g("nvfp4", z, z, z, z, 1.0, D, 64, 64, 64, "f32", config=fp4.GemmConfig(bn=48)) == 1
+    assert g("nvfp4", z, z, z, z, 1.0, D, 64, 64, 64, "f32", config=fp4.GemmConfig(cta_group=3)) == 1
+    assert g("nvfp4", z, z, z, z, 1.0, D, 64, 64, 64, "f32", config=fp4.GemmConfig(bn=64, cta_group=2)) == 2
     assert fp4.get_device_status() == 0
