@@ -18,11 +18,13 @@ from . import _build
 
 __all__ = ["FP4_OK", "Fp4Error", "load", "build", "gemm", "gemm_nvfp4", "gemm_mxfp4", "gemm_nvfp4_prepacked",
            "gemm_mxfp4_prepacked", "gemm_host", "scale_reorder", "scale_atom_bytes", "get_device_status",
-           "status_string", "set_wait_limit_ms", "GemmConfig", "FMT", "OUT"]
+           "status_string", "set_wait_limit_ms", "GemmConfig", "FMT", "OUT", "gemm_static_scratch",
+           "STATIC_SCRATCH_BYTES"]
 
 FP4_OK = 0
 STATUS_NAMES = {0: "FP4_OK", 1: "FP4_ERR_INVALID_ARG", 2: "FP4_ERR_UNSUPPORTED", 3: "FP4_ERR_MISALIGNED",
-                4: "FP4_ERR_CUDA", 5: "FP4_ERR_TIMEOUT", 6: "FP4_ERR_NO_DEVICE"}
+                4: "FP4_ERR_CUDA", 5: "FP4_ERR_TIMEOUT", 6: "FP4_ERR_NO_DEVICE", 7: "FP4_ERR_SCRATCH_LIMIT"}
+STATIC_SCRATCH_BYTES = 16 << 20
 FMT = {"nvfp4": 0, "mxfp4": 1}
 OUT = {"f32": 0, "bf16": 1}
 
@@ -64,6 +66,8 @@ def load():
     lib.fp4_gemm.restype = i32
     lib.fp4_gemm_host.argtypes = [i32, vp, vp, vp, vp, f32, vp, i64, i64, i64, i32, vp]
     lib.fp4_gemm_host.restype = i32
+    lib.fp4_gemm_static_scratch.argtypes = [i32, vp, vp, vp, vp, f32, vp, i64, i64, i64, i32, vp]
+    lib.fp4_gemm_static_scratch.restype = i32
     lib.fp4_scale_atom_bytes.argtypes = [i64, i64, i32]
     lib.fp4_scale_atom_bytes.restype = ctypes.c_size_t
     lib.fp4_scale_reorder.argtypes = [vp, vp, i64, i64, i32, vp]
@@ -143,6 +147,17 @@ def gemm_host(fmt: str, A, sfA, B, sfB, alpha: float, D, M: int, N: int, K: int,
                               int(N), int(K), OUT[out], _stream(stream))
     if check:
         _check(st, "fp4_gemm_host")
+    return st
+
+
+def gemm_static_scratch(fmt: str, A, sfA, B, sfB, alpha: float, D, M: int, N: int, K: int, out: str = "f32",
+                        stream=None, check: bool = True) -> int:
+    """fp4_gemm_static_scratch: plain-scale GEMM for callers that must not allocate;
+    its scratch is the library's static 16 MiB device array (see the header)."""
+    st = load().fp4_gemm_static_scratch(FMT[fmt], _ptr(A), _ptr(sfA), _ptr(B), _ptr(sfB), float(alpha), _ptr(D),
+                                        int(M), int(N), int(K), OUT[out], _stream(stream))
+    if check:
+        _check(st, "fp4_gemm_static_scratch")
     return st
 
 

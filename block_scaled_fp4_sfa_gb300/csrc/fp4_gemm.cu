@@ -59,6 +59,12 @@ namespace fp4 {
 // Per-device status word: 0, or the first error a kernel recorded.
 __device__ int g_status;
 
+// Scratch of fp4_gemm_static_scratch (reordered scales, split-K partials) for
+// callers that cannot allocate. In host code this name is only a stand-in: its
+// device address comes from cudaGetSymbolAddress (static_scratch_address).
+constexpr size_t kStaticScratchBytes = FP4_STATIC_SCRATCH_BYTES;
+__device__ __align__(256) uint8_t g_static_scratch[kStaticScratchBytes];
+
 constexpr int kBM = 128;          // TMEM lanes / M rows per CTA
 constexpr int kBK = 256;          // FP4 elements per k-tile
 constexpr int kBKBytes = 128;     // bytes per row per k-tile
@@ -778,9 +784,12 @@ fp4_status reorder_launch(const void *sf_plain, void *sf_atom, int64_t rows, int
     return cudaGetLastError() == cudaSuccess ? FP4_OK : FP4_ERR_CUDA;
 }
 
+// `ext_scratch` (with `ext_bytes`), when given, replaces the stream-ordered
+// allocation of the call's scratch; a plan that needs more is refused.
 fp4_status gemm_impl(fp4_format fmt, int prepacked, const void *A, const void *sfA, const void *B,
                      const void *sfB, float alpha, void *D, int64_t M, int64_t N, int64_t K, fp4_out_dtype out,
-                     const fp4_gemm_config *cfg, cudaStream_t stream)
+                     const fp4_gemm_config *cfg, cudaStream_t stream, uint8_t *ext_scratch = nullptr,
+                     size_t ext_bytes = 0)
 {
     if (fmt != FP4_FMT_NVFP4 && fmt != FP4_FMT_MXFP4) return FP4_ERR_INVALID_ARG;
     if (out != FP4_OUT_F32 && out != FP4_OUT_BF16) return FP4_ERR_INVALID_ARG;
@@ -825,7 +834,10 @@ fp4_status gemm_impl(fp4_format fmt, int prepacked, const void *A, const void *s
     const size_t ws_bytes = plan.splits > 1 ? static_cast<size_t>(plan.splits) * rows_a * rows_b * 4 : 0;
     const size_t scratch_bytes = (prepacked ? 0 : atoms_a + atoms_b) + ws_bytes;
     uint8_t *scratch = nullptr;
-    if (scratch_bytes) {
+    if (ext_scratch) {
+        if (scratch_bytes > ext_bytes) return FP4_ERR_SCRATCH_LIMIT;
+        scratch = ext_scratch;
+    } else if (scratch_bytes) {
         if (cudaMallocAsync(reinterpret_cast<void **>(&scratch), scratch_bytes, stream) != cudaSuccess)
             return FP4_ERR_CUDA;
     }
@@ -911,8 +923,25 @@ fp4_status gemm_impl(fp4_format fmt, int prepacked, const void *A, const void *s
             }
         }
     } while (false);
-    if (scratch && cudaFreeAsync(scratch, stream) != cudaSuccess && result == FP4_OK) result = FP4_ERR_CUDA;
+    if (scratch && !ext_scratch && cudaFreeAsync(scratch, stream) != cudaSuccess && result == FP4_OK)
+        result = FP4_ERR_CUDA;
     return result;
+}
+
+// Device address of g_static_scratch on device `dev`, looked up once per
+// device (with that device current) and kept.
+uint8_t *g_static_scratch_addr[64] = {};
+
+fp4_status static_scratch_address(int dev, uint8_t **out)
+{
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_static_scratch_addr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || !p) return FP4_ERR_CUDA;
+        g_static_scratch_addr[dev] = static_cast<uint8_t *>(p);
+    }
+    *out = g_static_scratch_addr[dev];
+    return FP4_OK;
 }
 
 }  // namespace
@@ -987,6 +1016,20 @@ fp4_status fp4_gemm_host(fp4_format fmt, const void *A, const void *sfA, const v
     return st;
 }
 
+fp4_status fp4_gemm_static_scratch(fp4_format fmt, const void *A, const void *sfA, const void *B,
+                                   const void *sfB, float alpha, void *D, int64_t M, int64_t N, int64_t K,
+                                   fp4_out_dtype out, cudaStream_t stream)
+{
+    int dev;
+    DeviceInfo *info;
+    fp4_status st = device_info(dev, info);
+    if (st != FP4_OK) return st;
+    uint8_t *scratch = nullptr;
+    if ((st = static_scratch_address(dev, &scratch)) != FP4_OK) return st;
+    return gemm_impl(fmt, 0, A, sfA, B, sfB, alpha, D, M, N, K, out, nullptr, stream, scratch,
+                     kStaticScratchBytes);
+}
+
 size_t fp4_scale_atom_bytes(int64_t rows, int64_t k, int vec)
 {
     if (rows < 0 || k < 0 || (vec != 16 && vec != 32) || k % vec != 0) return 0;
@@ -1030,6 +1073,7 @@ const char *fp4_status_string(fp4_status s)
     case FP4_ERR_CUDA: return "CUDA call failed";
     case FP4_ERR_TIMEOUT: return "bounded device wait ran out";
     case FP4_ERR_NO_DEVICE: return "no sm_103 device";
+    case FP4_ERR_SCRATCH_LIMIT: return "problem needs more than the 16 MiB static scratch array";
     default: return "unknown status";
     }
 }

@@ -63,7 +63,8 @@ typedef enum {
     FP4_ERR_MISALIGNED = 3,    /* a pointer not 16-byte aligned */
     FP4_ERR_CUDA = 4,          /* a CUDA runtime/driver call failed */
     FP4_ERR_TIMEOUT = 5,       /* a bounded device wait ran out (reported by fp4_get_device_status) */
-    FP4_ERR_NO_DEVICE = 6      /* no device, or not an sm_103 device */
+    FP4_ERR_NO_DEVICE = 6,     /* no device, or not an sm_103 device */
+    FP4_ERR_SCRATCH_LIMIT = 7  /* fp4_gemm_static_scratch: problem needs more than FP4_STATIC_SCRATCH_BYTES */
 } fp4_status;
 
 typedef enum { FP4_OUT_F32 = 0, FP4_OUT_BF16 = 1 } fp4_out_dtype;
@@ -119,6 +120,33 @@ fp4_status fp4_gemm(fp4_format fmt, int scales_prepacked, const void *A, const v
 fp4_status fp4_gemm_host(fp4_format fmt, const void *A, const void *sfA, const void *B,
                          const void *sfB, float alpha, void *D, int64_t M, int64_t N, int64_t K,
                          fp4_out_dtype out, cudaStream_t stream);
+
+/* Capacity of the library's static device scratch array (see fp4_gemm_static_scratch). */
+#define FP4_STATIC_SCRATCH_BYTES (16u << 20)
+
+/* The same GEMM as fp4_gemm_nvfp4 / fp4_gemm_mxfp4 (plain row-major scales),
+ * for callers that must not allocate device memory: code running where
+ * cudaMalloc / cudaMallocAsync are unavailable or forbidden, such as inside a
+ * memory-pool owner, an allocator callback, or a process whose device memory
+ * is entirely pre-reserved by another framework. The pages have no
+ * counterpart; this entry point exists for such callers only.
+ *
+ * The reordered scales and any split-K partial sums go to one static
+ * __device__ array of FP4_STATIC_SCRATCH_BYTES (16 MiB) that every device
+ * loading the library holds until the process exits. Problems whose scratch
+ * does not fit (2 * ceil(rows/128) * ceil(K/vec/4) * 512 bytes of atoms plus,
+ * for split-K plans, splits * M * N * 4 bytes) are rejected with
+ * FP4_ERR_SCRATCH_LIMIT before anything is launched. The call allocates
+ * nothing and calls no allocating library routine. Nothing in the array has
+ * to start at zero: every byte a call reads was written earlier in the same
+ * call. All calls on a device share the array, so calls whose kernels overlap
+ * on the GPU (other streams, other threads) race: order them on one stream.
+ * The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture. Inputs, outputs and errors as fp4_gemm. */
+fp4_status fp4_gemm_static_scratch(fp4_format fmt, const void *A, const void *sfA, const void *B,
+                                   const void *sfB, float alpha, void *D, int64_t M, int64_t N,
+                                   int64_t K, fp4_out_dtype out, cudaStream_t stream);
 
 /* Bytes of the atom-layout copy of a rows x (k/vec) scale matrix (vec 16 or 32).
  * Returns 0 for invalid arguments. */
