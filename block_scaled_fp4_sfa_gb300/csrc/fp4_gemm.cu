@@ -71,14 +71,13 @@ constexpr int kBKBytes = 128;     // bytes per row per k-tile
 constexpr int kAtomBytes = 512;   // one 128-row x 4-column scale atom
 constexpr int kEpiWarps = 8;
 constexpr int kThreads = 64 + 32 * kEpiWarps;   // producer warp, MMA warp, epilogue warps
-constexpr int kStgBytes = 32 * 128;             // per-warp store box: 32 rows x 128 bytes
 constexpr int kSmemLimit = 232448;
 
-enum EpiMode : int32_t { kEpiTmaStore = 0, kEpiTransposed = 1, kEpiSplitK = 2 };
+enum EpiMode : int32_t { kEpiRows = 0, kEpiTransposed = 1, kEpiSplitK = 2 };
 
 struct Args {
     void *out;               // D (modes 0, 1) or split-K workspace (mode 2)
-    int64_t ldo;             // row stride in elements of `out` for modes 1 and 2
+    int64_t ldo;             // row stride in elements of `out`
     int64_t split_stride;    // elements between split partials (mode 2)
     uint64_t wait_ns;        // bound on every mbarrier wait
     int32_t rows_a, rows_b;
@@ -90,43 +89,45 @@ struct Args {
     float alpha;
 };
 
-template <int CG, int BN, bool MX>
+template <int CG, int BN, bool MX, int KT>
 struct Cfg {
     static constexpr int APK = MX ? 2 : 4;             // scale atoms per k-tile per 128-row block
     static constexpr int NRB = (BN + 127) / 128;       // 128-row scale blocks on the N side (whole tile)
     static constexpr int BN_CTA = BN / CG;             // N-side rows loaded by one CTA
+    // one k-tile slot of shared memory
     static constexpr int A_BYTES = kBM * kBKBytes;      // 16 KB
     static constexpr int B_BYTES = BN_CTA * kBKBytes;
     static constexpr int SFA_BYTES = APK * kAtomBytes;
     static constexpr int SFB_BYTES = NRB * APK * kAtomBytes;
-    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
-    static constexpr int STAGING_BYTES = kEpiWarps * kStgBytes;
+    static constexpr int KTILE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
+    // a stage is KT consecutive k-tile slots, filled by one TMA load per operand
+    static constexpr int STAGE_BYTES = KT * KTILE_BYTES;
     static constexpr int BAR_BYTES = 256;
-    static constexpr int BUDGET = kSmemLimit - 1024 - BAR_BYTES - STAGING_BYTES;
+    static constexpr int BUDGET = kSmemLimit - 1024 - BAR_BYTES;
     static constexpr int STAGES_FIT = BUDGET / STAGE_BYTES;
-    static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
+    static constexpr int STAGES = STAGES_FIT * KT > 8 ? 8 / KT : STAGES_FIT;
+    static constexpr int SLOTS = STAGES * KT;                   // k-tile slots in the ring
     static constexpr int ACC_BUFS = BN <= 128 ? 2 : 1;
-    static constexpr int SF_COLS = 4 * APK * (1 + NRB);   // TMEM columns of one stage's scales
-    static constexpr int SF_TMEM = ACC_BUFS * BN;          // first scale column
-    static constexpr int TMEM_USED = ACC_BUFS * BN + STAGES * SF_COLS;
+    static constexpr int SF_COLS = 4 * APK * (1 + NRB);        // TMEM columns of one k-tile's scales
+    static constexpr int SF_TMEM = ACC_BUFS * BN;               // first scale column
+    static constexpr int TMEM_USED = ACC_BUFS * BN + SLOTS * SF_COLS;
     static constexpr int TMEM_COLS = TMEM_USED <= 32 ? 32 : TMEM_USED <= 64 ? 64 : TMEM_USED <= 128 ? 128
                                    : TMEM_USED <= 256 ? 256 : 512;
-    static constexpr int OFF_A = 0;
-    static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
-    static constexpr int OFF_SFA = OFF_B + STAGES * B_BYTES;
-    static constexpr int OFF_SFB = OFF_SFA + STAGES * SFA_BYTES;
-    static constexpr int OFF_STG = OFF_SFB + STAGES * SFB_BYTES;
-    static constexpr int OFF_BAR = OFF_STG + STAGING_BYTES;
+    static constexpr int OFF_A = 0;                              // slot k at OFF_X + k * X_BYTES
+    static constexpr int OFF_B = OFF_A + SLOTS * A_BYTES;
+    static constexpr int OFF_SFA = OFF_B + SLOTS * B_BYTES;
+    static constexpr int OFF_SFB = OFF_SFA + SLOTS * SFA_BYTES;
+    static constexpr int OFF_BAR = OFF_SFB + SLOTS * SFB_BYTES;
     static constexpr int SMEM_BYTES = OFF_BAR + BAR_BYTES + 1024;   // + alignment slack
     static constexpr int COLS_WARP = BN / 2;                        // accumulator columns per epilogue warp
     static constexpr uint32_t TX_BYTES = CG * STAGE_BYTES;          // bytes landing per stage (both CTAs)
     static_assert(CG == 1 || CG == 2, "CTA group of 1 or 2");
+    static_assert(KT == 1 || KT == 2, "one or two k-tiles per stage");
     static_assert(CG == 1 || BN >= 128, "paired CTAs use N tiles of 128 or 256");
     static_assert(STAGES >= 2, "too few pipeline stages");
     static_assert(TMEM_USED <= 512, "TMEM budget exceeded");
     static_assert(SMEM_BYTES <= kSmemLimit, "shared memory budget exceeded");
     static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N must be a multiple of 16 in [16, 256]");
-    static_assert(OFF_STG % 1024 == 0 && kStgBytes % 1024 == 0, "swizzled staging must be 1024-aligned");
 };
 
 // Records the first error of this device (later ones are dropped).
@@ -199,13 +200,13 @@ __device__ __forceinline__ void tmem_load_cols(uint32_t taddr, uint32_t *v)
     }
 }
 
-template <int CG, int BN, bool MX>
+template <int CG, int BN, bool MX, int KT>
 __global__ void __launch_bounds__(kThreads, 1)
     fp4_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                     const __grid_constant__ CUtensorMap tmap_sfa, const __grid_constant__ CUtensorMap tmap_sfb,
-                    const __grid_constant__ CUtensorMap tmap_d, const Args args)
+                    const Args args)
 {
-    using C = Cfg<CG, BN, MX>;
+    using C = Cfg<CG, BN, MX, KT>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -244,7 +245,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         prefetch_tensormap(&tmap_b);
         prefetch_tensormap(&tmap_sfa);
         prefetch_tensormap(&tmap_sfb);
-        if (args.mode == kEpiTmaStore) prefetch_tensormap(&tmap_d);
     }
     if (warp == 1) {
         tmem_alloc<CG>(smem_u32(tmem_holder), C::TMEM_COLS);
@@ -274,19 +274,29 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int row_a = rba * kBM;
                 const int row_b = tb * BN + static_cast<int>(rank) * C::BN_CTA;
                 const int rbb = (tb * BN) / 128;                         // first scale block of the N side
-                for (int kt = kt0; kt < kt1; ++kt) {
+                for (int kt = kt0; kt < kt1; kt += KT) {
                     if (!wait(bar_empty + 8 * stage, phase ^ 1u, args.wait_ns, abort_flag)) {
                         ok = false;
                         break;
                     }
                     const uint32_t full = full0 + 8 * stage;                 // shared::cluster address
                     if (rank == 0) mbar_arrive_expect_tx(bar_full + 8 * stage, C::TX_BYTES);
-                    tma_load_2d<CG>(base + C::OFF_A + stage * C::A_BYTES, &tmap_a, full, kt * kBKBytes, row_a);
-                    tma_load_2d<CG>(base + C::OFF_B + stage * C::B_BYTES, &tmap_b, full, kt * kBKBytes, row_b);
-                    tma_load_2d<CG>(base + C::OFF_SFA + stage * C::SFA_BYTES, &tmap_sfa, full,
-                                    kt * C::APK * (kAtomBytes / 8), rba);
-                    tma_load_2d<CG>(base + C::OFF_SFB + stage * C::SFB_BYTES, &tmap_sfb, full,
-                                    kt * C::APK * (kAtomBytes / 8), rbb);
+                    const int slot = stage * KT;
+                    if constexpr (KT == 1) {
+                        tma_load_2d<CG>(base + C::OFF_A + slot * C::A_BYTES, &tmap_a, full, kt * kBKBytes, row_a);
+                        tma_load_2d<CG>(base + C::OFF_B + slot * C::B_BYTES, &tmap_b, full, kt * kBKBytes, row_b);
+                        tma_load_2d<CG>(base + C::OFF_SFA + slot * C::SFA_BYTES, &tmap_sfa, full,
+                                        kt * C::APK * (kAtomBytes / 8), rba);
+                        tma_load_2d<CG>(base + C::OFF_SFB + slot * C::SFB_BYTES, &tmap_sfb, full,
+                                        kt * C::APK * (kAtomBytes / 8), rbb);
+                    } else {
+                        // 3-D views with the k-tile as the outer coordinate: one load per
+                        // operand fills KT consecutive k-tile slots (past K: zero fill)
+                        tma_load_3d<CG>(base + C::OFF_A + slot * C::A_BYTES, &tmap_a, full, 0, row_a, kt);
+                        tma_load_3d<CG>(base + C::OFF_B + slot * C::B_BYTES, &tmap_b, full, 0, row_b, kt);
+                        tma_load_3d<CG>(base + C::OFF_SFA + slot * C::SFA_BYTES, &tmap_sfa, full, 0, rba, kt);
+                        tma_load_3d<CG>(base + C::OFF_SFB + slot * C::SFB_BYTES, &tmap_sfb, full, 0, rbb, kt);
+                    }
                     filled |= 1u << stage;
                     fill_parity = (fill_parity & ~(1u << stage)) | (phase << stage);
                     if (++stage == C::STAGES) {
@@ -328,31 +338,37 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!wait(bar_acc_empty + 8 * acc, acc_phase ^ 1u, args.wait_ns, abort_flag)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem + static_cast<uint32_t>(acc * BN);
-                for (int kt = kt0; kt < kt1; ++kt) {
+                for (int kt = kt0; kt < kt1; kt += KT) {
                     if (!wait(bar_full + 8 * stage, phase, args.wait_ns, abort_flag)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t sf = tmem + static_cast<uint32_t>(C::SF_TMEM + stage * C::SF_COLS);
-                    const uint64_t dsa = desc_sfa0 + static_cast<uint64_t>((stage * C::SFA_BYTES) >> 4);
-                    const uint64_t dsb = desc_sfb0 + static_cast<uint64_t>((stage * C::SFB_BYTES) >> 4);
 #pragma unroll
-                    for (int t = 0; t < C::APK; ++t) {
-                        tc_cp_32x128b_warpx4<CG>(sf + 4 * t, dsa + (t * kAtomBytes >> 4));
+                    for (int j = 0; j < KT; ++j) {
+                        if (KT > 1 && kt + j >= kt1) break;              // last stage of an odd k range
+                        const int slot = stage * KT + j;
+                        const uint32_t sf = tmem + static_cast<uint32_t>(C::SF_TMEM + slot * C::SF_COLS);
+                        const uint64_t dsa = desc_sfa0 + static_cast<uint64_t>((slot * C::SFA_BYTES) >> 4);
+                        const uint64_t dsb = desc_sfb0 + static_cast<uint64_t>((slot * C::SFB_BYTES) >> 4);
 #pragma unroll
-                        for (int rb = 0; rb < C::NRB; ++rb)
-                            tc_cp_32x128b_warpx4<CG>(sf + 4 * C::APK + 4 * (t * C::NRB + rb),
-                                                     dsb + ((rb * C::APK + t) * kAtomBytes >> 4));
-                    }
-                    const uint64_t da = desc_a0 + static_cast<uint64_t>((stage * C::A_BYTES) >> 4);
-                    const uint64_t db = desc_b0 + static_cast<uint64_t>((stage * C::B_BYTES) >> 4);
+                        for (int t = 0; t < C::APK; ++t) {
+                            tc_cp_32x128b_warpx4<CG>(sf + 4 * t, dsa + (t * kAtomBytes >> 4));
 #pragma unroll
-                    for (int j = 0; j < kBK / 64; ++j) {
-                        const int t = MX ? (j >> 1) : j;
-                        const uint32_t idesc = (MX && (j & 1)) ? ID2 : ID0;
-                        tc_mma_fp4<CG, MX>(d_tmem, da + 2 * j, db + 2 * j, idesc, sf + 4 * t,
-                                           sf + 4 * C::APK + 4 * C::NRB * t, (kt > kt0 || j > 0) ? 1u : 0u);
+                            for (int rb = 0; rb < C::NRB; ++rb)
+                                tc_cp_32x128b_warpx4<CG>(sf + 4 * C::APK + 4 * (t * C::NRB + rb),
+                                                         dsb + ((rb * C::APK + t) * kAtomBytes >> 4));
+                        }
+                        const uint64_t da = desc_a0 + static_cast<uint64_t>((slot * C::A_BYTES) >> 4);
+                        const uint64_t db = desc_b0 + static_cast<uint64_t>((slot * C::B_BYTES) >> 4);
+#pragma unroll
+                        for (int i = 0; i < kBK / 64; ++i) {
+                            const int t = MX ? (i >> 1) : i;
+                            const uint32_t idesc = (MX && (i & 1)) ? ID2 : ID0;
+                            tc_mma_fp4<CG, MX>(d_tmem, da + 2 * i, db + 2 * i, idesc, sf + 4 * t,
+                                               sf + 4 * C::APK + 4 * C::NRB * t,
+                                               (kt + j > kt0 || i > 0) ? 1u : 0u);
+                        }
                     }
                     tc_commit<CG>(bar_empty + 8 * stage);
                     if (++stage == C::STAGES) {
@@ -378,8 +394,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int q = warp & 3;                          // TMEM lane quarter of this warp
         const int h = (warp - 2) >> 2;                   // which half of the tile's columns
         const uint32_t acc_empty0 = CG == 2 ? mapa_shared(bar_acc_empty, 0) : bar_acc_empty;
-        const uint32_t stg = base + C::OFF_STG + (warp - 2) * kStgBytes;
-        uint8_t *const stg_ptr = base_ptr + C::OFF_STG + (warp - 2) * kStgBytes;
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int u = pair; u < args.units; u += npairs) {
@@ -401,65 +415,60 @@ __global__ void __launch_bounds__(kThreads, 1)
                 else
                     mbar_arrive(bar_acc_empty + 8 * acc);
             }
-            const int row_a0 = (ta * CG + static_cast<int>(rank)) * kBM + 32 * q;   // this warp's first row
-            const int col0 = tb * BN + h * C::COLS_WARP;
-            if (args.mode == kEpiTmaStore) {
-                if constexpr (C::COLS_WARP >= 64) {
-                    const int cw = args.bf16 ? 64 : 32;                 // columns per 128-byte box row
-                    const int nch = C::COLS_WARP / cw;
-                    for (int ch = 0; ch < nch; ++ch) {
-                        uint32_t w[32];
-                        if (args.bf16) {
+            const int ra = (ta * CG + static_cast<int>(rank)) * kBM + 32 * q + lane;   // slot-A row of this lane
+            const int col0 = tb * BN + h * C::COLS_WARP;                                // first slot-B row
+            if (ra < args.rows_a) {
+                if (args.mode == kEpiRows) {
+                    // D row ra, columns col0...: 16-byte stores (the row pitch is a
+                    // multiple of 16 bytes and N of 4 (fp32) or 8 (bf16) elements)
+                    if (args.bf16) {
+                        uint4 *d = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(args.out) +
+                                                             static_cast<int64_t>(ra) * args.ldo + col0);
 #pragma unroll
-                            for (int i = 0; i < 32; ++i) {
-                                const int c = ch * 64 + 2 * i;
-                                __nv_bfloat162 p = __floats2bfloat162_rn(__uint_as_float(v[c]) * args.alpha,
-                                                                         __uint_as_float(v[c + 1]) * args.alpha);
-                                w[i] = *reinterpret_cast<uint32_t *>(&p);
+                        for (int c = 0; c < C::COLS_WARP / 8; ++c) {
+                            if (col0 + 8 * c < args.rows_b) {
+                                uint32_t w[4];
+#pragma unroll
+                                for (int i = 0; i < 4; ++i) {
+                                    __nv_bfloat162 p = __floats2bfloat162_rn(
+                                        __uint_as_float(v[8 * c + 2 * i]) * args.alpha,
+                                        __uint_as_float(v[8 * c + 2 * i + 1]) * args.alpha);
+                                    w[i] = *reinterpret_cast<uint32_t *>(&p);
+                                }
+                                d[c] = make_uint4(w[0], w[1], w[2], w[3]);
                             }
-                        } else {
-#pragma unroll
-                            for (int i = 0; i < 32; ++i)
-                                w[i] = __float_as_uint(__uint_as_float(v[ch * 32 + i]) * args.alpha);
                         }
-                        if (lane == 0) bulk_wait_group_read<0>();       // the box buffer is free again
-                        __syncwarp();
-#pragma unroll
-                        for (int c = 0; c < 8; ++c)
-                            *reinterpret_cast<uint4 *>(stg_ptr + lane * 128 + ((c ^ (lane & 7)) << 4)) =
-                                make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
-                        fence_proxy_async_smem();
-                        __syncwarp();
-                        if (lane == 0) {
-                            tma_store_2d(&tmap_d, stg, col0 + ch * cw, row_a0);
-                            bulk_commit_group();
-                        }
-                    }
-                }
-            } else {
-                // Transposed direct stores (swap-AB) or fp32 split-K partials: for a
-                // fixed column the 32 lanes of a warp write 32 consecutive elements.
-                const int ra = row_a0 + lane;
-                if (ra < args.rows_a) {
-                    if (args.mode == kEpiSplitK) {
-                        float *ws = static_cast<float *>(args.out) + split * args.split_stride + ra;
-#pragma unroll
-                        for (int i = 0; i < C::COLS_WARP; ++i)
-                            if (col0 + i < args.rows_b) ws[static_cast<int64_t>(col0 + i) * args.ldo] = __uint_as_float(v[i]);
-                    } else if (args.bf16) {
-                        __nv_bfloat16 *d = static_cast<__nv_bfloat16 *>(args.out) + ra;
-#pragma unroll
-                        for (int i = 0; i < C::COLS_WARP; ++i)
-                            if (col0 + i < args.rows_b)
-                                d[static_cast<int64_t>(col0 + i) * args.ldo] =
-                                    __float2bfloat16_rn(__uint_as_float(v[i]) * args.alpha);
                     } else {
-                        float *d = static_cast<float *>(args.out) + ra;
+                        float4 *d = reinterpret_cast<float4 *>(static_cast<float *>(args.out) +
+                                                               static_cast<int64_t>(ra) * args.ldo + col0);
 #pragma unroll
-                        for (int i = 0; i < C::COLS_WARP; ++i)
-                            if (col0 + i < args.rows_b)
-                                d[static_cast<int64_t>(col0 + i) * args.ldo] = __uint_as_float(v[i]) * args.alpha;
+                        for (int c = 0; c < C::COLS_WARP / 4; ++c)
+                            if (col0 + 4 * c < args.rows_b)
+                                d[c] = make_float4(__uint_as_float(v[4 * c]) * args.alpha,
+                                                   __uint_as_float(v[4 * c + 1]) * args.alpha,
+                                                   __uint_as_float(v[4 * c + 2]) * args.alpha,
+                                                   __uint_as_float(v[4 * c + 3]) * args.alpha);
                     }
+                } else if (args.mode == kEpiSplitK) {
+                    // fp32 partials, transposed: for a fixed column the 32 lanes of a
+                    // warp write 32 consecutive elements
+                    float *ws = static_cast<float *>(args.out) + split * args.split_stride + ra;
+#pragma unroll
+                    for (int i = 0; i < C::COLS_WARP; ++i)
+                        if (col0 + i < args.rows_b) ws[static_cast<int64_t>(col0 + i) * args.ldo] = __uint_as_float(v[i]);
+                } else if (args.bf16) {
+                    __nv_bfloat16 *d = static_cast<__nv_bfloat16 *>(args.out) + ra;
+#pragma unroll
+                    for (int i = 0; i < C::COLS_WARP; ++i)
+                        if (col0 + i < args.rows_b)
+                            d[static_cast<int64_t>(col0 + i) * args.ldo] =
+                                __float2bfloat16_rn(__uint_as_float(v[i]) * args.alpha);
+                } else {
+                    float *d = static_cast<float *>(args.out) + ra;
+#pragma unroll
+                    for (int i = 0; i < C::COLS_WARP; ++i)
+                        if (col0 + i < args.rows_b)
+                            d[static_cast<int64_t>(col0 + i) * args.ldo] = __uint_as_float(v[i]) * args.alpha;
                 }
             }
             if (C::ACC_BUFS == 2) {
@@ -469,7 +478,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 acc_phase ^= 1u;
             }
         }
-        if (lane == 0) bulk_wait_group<0>();
     }
 
     __syncwarp();
@@ -543,8 +551,7 @@ std::mutex g_mu;
 int64_t g_wait_ms = -1;
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
-constexpr int kNumKernels = 14;   // (CTA group 1: five widths + group 2: two widths) x two formats
-
+constexpr int kNumKernels = 20;   // kernel variants that can be launched (see kernel_index)
 struct DeviceInfo {
     bool probed = false;
     bool ok = false;
@@ -593,15 +600,53 @@ fp4_status device_info(int &dev, DeviceInfo *&info)
     return FP4_OK;
 }
 
-bool encode_2d(CUtensorMap *m, CUtensorMapDataType dt, const void *ptr, uint64_t inner, uint64_t outer,
-               uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw)
+bool encode(CUtensorMap *m, CUtensorMapDataType dt, int rank, const void *ptr, const cuuint64_t *dims,
+            const cuuint64_t *strides, const cuuint32_t *box, CUtensorMapSwizzle sw)
 {
-    const cuuint64_t dims[2] = {inner, outer};
-    const cuuint64_t strides[1] = {row_bytes};
-    const cuuint32_t box[2] = {box_inner, box_outer};
-    const cuuint32_t estr[2] = {1, 1};
-    return g_encode(m, dt, 2, const_cast<void *>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return g_encode(m, dt, rank, const_cast<void *>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Operand map: rows x K/2 bytes, box of `box_rows` rows x one 128-byte k-tile
+// (2-D), or, with kt == 2, a 3-D view (byte in k-tile, row, k-tile) whose box
+// covers two consecutive k-tiles. 128-byte swizzle.
+bool encode_operand(CUtensorMap *m, const void *ptr, int64_t rows, int64_t K, int box_rows, int kt)
+{
+    if (kt == 1) {
+        const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K / 2), static_cast<cuuint64_t>(rows)};
+        const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K / 2)};
+        const cuuint32_t box[2] = {static_cast<cuuint32_t>(kBKBytes), static_cast<cuuint32_t>(box_rows)};
+        return encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, ptr, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+    }
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kBKBytes), static_cast<cuuint64_t>(rows),
+                                static_cast<cuuint64_t>(K / kBK)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(K / 2), static_cast<cuuint64_t>(kBKBytes)};
+    const cuuint32_t box[3] = {static_cast<cuuint32_t>(kBKBytes), static_cast<cuuint32_t>(box_rows),
+                               static_cast<cuuint32_t>(kt)};
+    return encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, ptr, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+// Scale-atom map: the atom buffer as int64 rows of ceil(K/vec/4) * 64 elements
+// per 128-row block; a box is one k-tile's atoms of `box_blocks` blocks (2-D),
+// or, with kt == 2, a 3-D view (element in k-tile, block, k-tile) covering two
+// k-tiles. Past the matrix the box is zero-filled.
+bool encode_scales(CUtensorMap *m, const void *atoms, int64_t row_blocks, int64_t kc4, int apk, int box_blocks,
+                   int kt, int64_t k_tiles)
+{
+    if (kt == 1) {
+        const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kc4 * 64), static_cast<cuuint64_t>(row_blocks)};
+        const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kc4 * kAtomBytes)};
+        const cuuint32_t box[2] = {static_cast<cuuint32_t>(apk * 64), static_cast<cuuint32_t>(box_blocks)};
+        return encode(m, CU_TENSOR_MAP_DATA_TYPE_INT64, 2, atoms, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
+    }
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(apk * 64), static_cast<cuuint64_t>(row_blocks),
+                                static_cast<cuuint64_t>(k_tiles)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(kc4 * kAtomBytes),
+                                   static_cast<cuuint64_t>(apk * kAtomBytes)};
+    const cuuint32_t box[3] = {static_cast<cuuint32_t>(apk * 64), static_cast<cuuint32_t>(box_blocks),
+                               static_cast<cuuint32_t>(kt)};
+    return encode(m, CU_TENSOR_MAP_DATA_TYPE_INT64, 3, atoms, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -620,15 +665,15 @@ int bn_index(int bn)
 }
 
 struct Maps {
-    CUtensorMap a, b, sfa, sfb, d;
+    CUtensorMap a, b, sfa, sfb;
 };
 
-template <int CG, int BN, bool MX>
+template <int CG, int BN, bool MX, int KT>
 cudaError_t launch_gemm(DeviceInfo &info, int kidx, int units, int cap, const Maps &m, const Args &args,
                         cudaStream_t stream)
 {
-    using C = Cfg<CG, BN, MX>;
-    auto kern = fp4_gemm_kernel<CG, BN, MX>;
+    using C = Cfg<CG, BN, MX, KT>;
+    auto kern = fp4_gemm_kernel<CG, BN, MX, KT>;
     cudaLaunchAttribute cluster_attr[1];
     cluster_attr[0].id = cudaLaunchAttributeClusterDimension;
     cluster_attr[0].val.clusterDim.x = CG;
@@ -668,38 +713,52 @@ cudaError_t launch_gemm(DeviceInfo &info, int kidx, int units, int cap, const Ma
         lc.attrs = cluster_attr;
         lc.numAttrs = 1;
     }
-    return cudaLaunchKernelEx(&lc, kern, m.a, m.b, m.sfa, m.sfb, m.d, args);
+    return cudaLaunchKernelEx(&lc, kern, m.a, m.b, m.sfa, m.sfb, args);
 }
 
-cudaError_t launch_by_cfg(int cg, int bn, bool mx, DeviceInfo &info, int units, int cap, const Maps &m,
+// Variants: one CTA: N 16..256, pair: N 128 / 256; each for both formats, with
+// one k-tile per stage; pairs with MXFP4 also with two k-tiles per stage.
+int kernel_index(int cg, int bn, bool mx, int kt)
+{
+    if (cg == 1) return bn_index(bn) * 2 + (mx ? 1 : 0);                   // 0..9
+    const int w = bn == 256 ? 1 : 0;
+    if (kt == 1) return 10 + w * 2 + (mx ? 1 : 0);                          // 10..13
+    return 14 + w;                                                          // 14..15 (MXFP4)
+}
+
+cudaError_t launch_by_cfg(int cg, int bn, bool mx, int kt, DeviceInfo &info, int units, int cap, const Maps &m,
                           const Args &args, cudaStream_t stream)
 {
-    const int k = (cg == 2 ? 10 + (bn == 256 ? 2 : 0) : bn_index(bn) * 2) + (mx ? 1 : 0);
-#define FP4_LAUNCH(CG_, BN_, MX_) return launch_gemm<CG_, BN_, MX_>(info, k, units, cap, m, args, stream)
+    const int k = kernel_index(cg, bn, mx, kt);
+#define FP4_LAUNCH(CG_, BN_, MX_, KT_) return launch_gemm<CG_, BN_, MX_, KT_>(info, k, units, cap, m, args, stream)
     if (cg == 2) {
-        if (bn == 256) {
-            if (mx) FP4_LAUNCH(2, 256, true);
-            FP4_LAUNCH(2, 256, false);
+        if (kt == 2) {
+            if (bn == 256) FP4_LAUNCH(2, 256, true, 2);
+            FP4_LAUNCH(2, 128, true, 2);
         }
-        if (mx) FP4_LAUNCH(2, 128, true);
-        FP4_LAUNCH(2, 128, false);
+        if (bn == 256) {
+            if (mx) FP4_LAUNCH(2, 256, true, 1);
+            FP4_LAUNCH(2, 256, false, 1);
+        }
+        if (mx) FP4_LAUNCH(2, 128, true, 1);
+        FP4_LAUNCH(2, 128, false, 1);
     }
     switch (bn) {
     case 16:
-        if (mx) FP4_LAUNCH(1, 16, true);
-        FP4_LAUNCH(1, 16, false);
+        if (mx) FP4_LAUNCH(1, 16, true, 1);
+        FP4_LAUNCH(1, 16, false, 1);
     case 32:
-        if (mx) FP4_LAUNCH(1, 32, true);
-        FP4_LAUNCH(1, 32, false);
+        if (mx) FP4_LAUNCH(1, 32, true, 1);
+        FP4_LAUNCH(1, 32, false, 1);
     case 64:
-        if (mx) FP4_LAUNCH(1, 64, true);
-        FP4_LAUNCH(1, 64, false);
+        if (mx) FP4_LAUNCH(1, 64, true, 1);
+        FP4_LAUNCH(1, 64, false, 1);
     case 128:
-        if (mx) FP4_LAUNCH(1, 128, true);
-        FP4_LAUNCH(1, 128, false);
+        if (mx) FP4_LAUNCH(1, 128, true, 1);
+        FP4_LAUNCH(1, 128, false, 1);
     default:
-        if (mx) FP4_LAUNCH(1, 256, true);
-        FP4_LAUNCH(1, 256, false);
+        if (mx) FP4_LAUNCH(1, 256, true, 1);
+        FP4_LAUNCH(1, 256, false, 1);
     }
 #undef FP4_LAUNCH
 }
@@ -708,6 +767,7 @@ struct Plan {
     bool swap;
     int bn;
     int cg;
+    int kt;         // k-tiles per pipeline stage
     int splits;
     int cap;
 };
@@ -721,9 +781,11 @@ int pow2_bn(int64_t rows)
     return 256;
 }
 
-// Chooses direct vs swap-AB, the tile N, the CTA group and the K split.
-// `tma_ok` says whether D's rows can take TMA stores (pitch 16-byte aligned).
-fp4_status make_plan(int64_t M, int64_t N, int64_t K, bool tma_ok, int sms, const fp4_gemm_config *cfg, Plan &p)
+// Chooses direct vs swap-AB, the tile N, the CTA group, the K split and the
+// k-tiles per stage. `rows_ok` says whether D's rows take 16-byte vector stores
+// (pitch a multiple of 16 bytes), which direct mode needs.
+fp4_status make_plan(int64_t M, int64_t N, int64_t K, bool rows_ok, bool mx, int sms, const fp4_gemm_config *cfg,
+                     Plan &p)
 {
     const int mode = cfg ? cfg->mode : 0;
     if (mode < 0 || mode > 2) return FP4_ERR_INVALID_ARG;
@@ -732,13 +794,12 @@ fp4_status make_plan(int64_t M, int64_t N, int64_t K, bool tma_ok, int sms, cons
     else if (mode == 2)
         p.swap = true;
     else
-        p.swap = (M <= 256) || !tma_ok;
-    if (!p.swap && !tma_ok) return FP4_ERR_MISALIGNED;
+        p.swap = (M <= 256) || !rows_ok;
+    if (!p.swap && !rows_ok) return FP4_ERR_MISALIGNED;
     const int64_t rows_b = p.swap ? M : N;
     const int64_t rows_a = p.swap ? N : M;
     const int bn = (cfg && cfg->bn) ? cfg->bn : (p.swap ? pow2_bn(rows_b) : 256);
     if (bn_index(bn) < 0) return FP4_ERR_INVALID_ARG;
-    if (!p.swap && bn < 128) return FP4_ERR_UNSUPPORTED;           // direct mode stores 64-column warp boxes
     if (rows_b > bn && bn < 128) return FP4_ERR_UNSUPPORTED;       // N-side tiles must start on scale blocks
     p.bn = bn;
     const int cg = (cfg && cfg->cta_group) ? cfg->cta_group : ((bn >= 128 && rows_a > 128) ? 2 : 1);
@@ -768,6 +829,9 @@ fp4_status make_plan(int64_t M, int64_t N, int64_t K, bool tma_ok, int sms, cons
     }
     p.splits = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(splits, k_tiles)));
     p.cap = (cfg && cfg->max_ctas > 0) ? cfg->max_ctas : 0;
+    // Two k-tiles per TMA load where the producer would otherwise limit the MMA
+    // rate (MXFP4 pairs); the 3-D views need whole k-tiles (K % 256 == 0).
+    p.kt = (mx && cg == 2 && K % kBK == 0) ? 2 : 1;
     return FP4_OK;
 }
 
@@ -818,9 +882,9 @@ fp4_status gemm_impl(fp4_format fmt, int prepacked, const void *A, const void *s
     const int vec = mx ? 32 : 16;
     const int64_t ksf = K / vec;
     const int64_t kc4 = cdiv(ksf, 4);
-    const bool tma_ok = (N * esize) % 16 == 0;
+    const bool rows_ok = (N * esize) % 16 == 0;
     Plan plan;
-    st = make_plan(M, N, K, tma_ok, info->sms, cfg, plan);
+    st = make_plan(M, N, K, rows_ok, mx, info->sms, cfg, plan);
     if (st != FP4_OK) return st;
 
     const int64_t rows_a = plan.swap ? N : M, rows_b = plan.swap ? M : N;
@@ -854,23 +918,13 @@ fp4_status gemm_impl(fp4_format fmt, int prepacked, const void *A, const void *s
         }
         const int apk = mx ? 2 : 4;
         const int nrb = static_cast<int>(cdiv(plan.bn, 128));
+        const int64_t k_tiles = cdiv(K, kBK);
         Maps m;
         std::memset(&m, 0, sizeof m);
-        // Scale atoms are viewed as int64 rows of ceil(K/vec/4) * 64 elements per
-        // 128-row block; one box is one k-tile's atoms of 1 (slot A) or
-        // ceil(BN/128) (slot B) blocks, zero-filled past the matrix.
-        if (!encode_2d(&m.a, CU_TENSOR_MAP_DATA_TYPE_UINT8, op_a, static_cast<uint64_t>(K / 2),
-                       static_cast<uint64_t>(rows_a), static_cast<uint64_t>(K / 2), kBKBytes, kBM,
-                       CU_TENSOR_MAP_SWIZZLE_128B) ||
-            !encode_2d(&m.b, CU_TENSOR_MAP_DATA_TYPE_UINT8, op_b, static_cast<uint64_t>(K / 2),
-                       static_cast<uint64_t>(rows_b), static_cast<uint64_t>(K / 2), kBKBytes,
-                       static_cast<uint32_t>(plan.bn / plan.cg), CU_TENSOR_MAP_SWIZZLE_128B) ||
-            !encode_2d(&m.sfa, CU_TENSOR_MAP_DATA_TYPE_INT64, sfa_atoms, static_cast<uint64_t>(kc4 * 64),
-                       static_cast<uint64_t>(rb_a), static_cast<uint64_t>(kc4 * kAtomBytes),
-                       static_cast<uint32_t>(apk * 64), 1, CU_TENSOR_MAP_SWIZZLE_NONE) ||
-            !encode_2d(&m.sfb, CU_TENSOR_MAP_DATA_TYPE_INT64, sfb_atoms, static_cast<uint64_t>(kc4 * 64),
-                       static_cast<uint64_t>(rb_b), static_cast<uint64_t>(kc4 * kAtomBytes),
-                       static_cast<uint32_t>(apk * 64), static_cast<uint32_t>(nrb), CU_TENSOR_MAP_SWIZZLE_NONE)) {
+        if (!encode_operand(&m.a, op_a, rows_a, K, kBM, plan.kt) ||
+            !encode_operand(&m.b, op_b, rows_b, K, plan.bn / plan.cg, plan.kt) ||
+            !encode_scales(&m.sfa, sfa_atoms, rb_a, kc4, apk, 1, plan.kt, k_tiles) ||
+            !encode_scales(&m.sfb, sfb_atoms, rb_b, kc4, apk, nrb, plan.kt, k_tiles)) {
             result = FP4_ERR_CUDA;
             break;
         }
@@ -889,15 +943,9 @@ fp4_status gemm_impl(fp4_format fmt, int prepacked, const void *A, const void *s
         a.bf16 = out == FP4_OUT_BF16;
         a.alpha = alpha;
         if (!plan.swap) {
-            a.mode = kEpiTmaStore;
+            a.mode = kEpiRows;
             a.out = D;
-            const CUtensorMapDataType dt = a.bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
-            if (!encode_2d(&m.d, dt, D, static_cast<uint64_t>(N), static_cast<uint64_t>(M),
-                           static_cast<uint64_t>(N * esize), static_cast<uint32_t>(128 / esize), 32,
-                           CU_TENSOR_MAP_SWIZZLE_128B)) {
-                result = FP4_ERR_CUDA;
-                break;
-            }
+            a.ldo = N;
         } else if (a.splits > 1) {
             a.mode = kEpiSplitK;
             a.out = ws;
@@ -908,7 +956,7 @@ fp4_status gemm_impl(fp4_format fmt, int prepacked, const void *A, const void *s
             a.out = D;
             a.ldo = N;
         }
-        if (launch_by_cfg(plan.cg, plan.bn, mx, *info, a.units, plan.cap, m, a, stream) != cudaSuccess) {
+        if (launch_by_cfg(plan.cg, plan.bn, mx, plan.kt, *info, a.units, plan.cap, m, a, stream) != cudaSuccess) {
             result = FP4_ERR_CUDA;
             break;
         }

@@ -190,6 +190,7 @@ PLAN_CASES = [
     # or a CTA pair per MMA, split-K
     (1, 256, 0, 1), (1, 128, 0, 1), (1, 256, 0, 2), (1, 128, 0, 2), (2, 256, 0, 1), (2, 128, 0, 1),
     (2, 256, 0, 2), (2, 128, 2, 2), (2, 256, 3, 1), (2, 128, 2, 1), (2, 256, 3, 2), (1, 256, 0, 2),
+    (1, 64, 0, 1), (1, 32, 0, 1),
 ]
 
 
@@ -233,6 +234,16 @@ def test_k_tail_not_multiple_of_tile(fp4, orc):
             check_full(orc, inp, run(fp4, inp, fp4.GemmConfig(mode=2, bn=256)), "K=%d %s swap" % (K, fmt))
             check_full(orc, inp, run(fp4, inp, fp4.GemmConfig(mode=1, bn=128, cta_group=2)),
                        "K=%d %s pair" % (K, fmt))
+
+
+@pytest.mark.parametrize("K", [256, 768, 1280, 1792])
+def test_two_ktile_stages(fp4, orc, K):
+    # MXFP4 CTA pairs load two k-tiles per TMA box when K % 256 == 0; odd k-tile
+    # counts and split-K ranges end on a half-used stage
+    inp = W.make_random("mxfp4", 520, 384, K, out="bf16", seed=K)
+    check_full(orc, inp, run(fp4, inp, fp4.GemmConfig(mode=1, bn=256, cta_group=2)), "direct K=%d" % K)
+    check_full(orc, inp, run(fp4, inp, fp4.GemmConfig(mode=1, bn=128, cta_group=2)), "direct bn128 K=%d" % K)
+    check_full(orc, inp, run(fp4, inp, fp4.GemmConfig(mode=2, bn=256, cta_group=2, splits=3)), "split K=%d" % K)
 
 
 def test_prepacked_equals_plain(fp4, orc):
@@ -306,7 +317,7 @@ def test_error_statuses_launch_nothing(fp4):
     assert g("nvfp4", z, z, z, z, 1.0, D, -1, 64, 64, "f32") == 1
     assert g("nvfp4", None, z, z, z, 1.0, D, 64, 64, 64, "f32") == 1
     assert g("nvfp4", z[1:], z, z, z, 1.0, D, 64, 64, 64, "f32") == 3         # misaligned A
-    assert g("nvfp4", z, z, z, z, 1.0, D, 64, 64, 64, "f32", config=fp4.GemmConfig(mode=1, bn=64)) == 2
+    assert g("nvfp4", z, z, z, z, 1.0, D, 64, 300, 64, "f32", config=fp4.GemmConfig(mode=1, bn=64)) == 2
     assert g("nvfp4", z, z, z, z, 1.0, D, 64, 64, 64, "f32", config=fp4.GemmConfig(mode=1, splits=2)) == 2
     assert g("nvfp4", z, z, z, z, 1.0, D, 64, 64, 64, "f32", config=fp4.GemmConfig(bn=48)) == 1
     assert g("nvfp4", z, z, z, z, 1.0, D, 64, 64, 64, "f32", config=fp4.GemmConfig(cta_group=3)) == 1
