@@ -71,6 +71,7 @@ constexpr int kBKBytes = 128;     // bytes per row per k-tile
 constexpr int kAtomBytes = 512;   // one 128-row x 4-column scale atom
 constexpr int kEpiWarps = 8;
 constexpr int kThreads = 64 + 32 * kEpiWarps;   // producer warp, MMA warp, epilogue warps
+constexpr int kStgBytes = 32 * 32;              // per-warp store staging: 32 rows x 32 bytes
 constexpr int kSmemLimit = 232448;
 
 enum EpiMode : int32_t { kEpiRows = 0, kEpiTransposed = 1, kEpiSplitK = 2 };
@@ -103,7 +104,8 @@ struct Cfg {
     // a stage is KT consecutive k-tile slots, filled by one TMA load per operand
     static constexpr int STAGE_BYTES = KT * KTILE_BYTES;
     static constexpr int BAR_BYTES = 256;
-    static constexpr int BUDGET = kSmemLimit - 1024 - BAR_BYTES;
+    static constexpr int STAGING_BYTES = kEpiWarps * kStgBytes;     // 8 KB
+    static constexpr int BUDGET = kSmemLimit - 1024 - BAR_BYTES - STAGING_BYTES;
     static constexpr int STAGES_FIT = BUDGET / STAGE_BYTES;
     static constexpr int STAGES = STAGES_FIT * KT > 8 ? 8 / KT : STAGES_FIT;
     static constexpr int SLOTS = STAGES * KT;                   // k-tile slots in the ring
@@ -117,7 +119,8 @@ struct Cfg {
     static constexpr int OFF_B = OFF_A + SLOTS * A_BYTES;
     static constexpr int OFF_SFA = OFF_B + SLOTS * B_BYTES;
     static constexpr int OFF_SFB = OFF_SFA + SLOTS * SFA_BYTES;
-    static constexpr int OFF_BAR = OFF_SFB + SLOTS * SFB_BYTES;
+    static constexpr int OFF_STG = OFF_SFB + SLOTS * SFB_BYTES;
+    static constexpr int OFF_BAR = OFF_STG + STAGING_BYTES;
     static constexpr int SMEM_BYTES = OFF_BAR + BAR_BYTES + 1024;   // + alignment slack
     static constexpr int COLS_WARP = BN / 2;                        // accumulator columns per epilogue warp
     static constexpr uint32_t TX_BYTES = CG * STAGE_BYTES;          // bytes landing per stage (both CTAs)
@@ -198,6 +201,31 @@ __device__ __forceinline__ void tmem_load_cols(uint32_t taddr, uint32_t *v)
             tmem_ld_32x32b_x32(taddr + 32 * c, r);
         }
     }
+}
+
+// One warp stores a 32-row x 32-byte chunk of D: lane l holds row row0 + l's
+// 32 bytes in w[]; they go through the warp's 1 KB staging (16-byte halves
+// swapped on every 4th row against bank conflicts) so that each store
+// instruction writes 16 rows x 32 bytes, i.e. whole sectors. `half_cols` is the
+// element count of 16 bytes.
+__device__ __forceinline__ void store_chunk32(uint8_t *stg, const uint32_t (&w)[8], void *out, int64_t ldo,
+                                              int esize, int row0, int col0, int half_cols, int rows, int cols,
+                                              int lane)
+{
+    const int sw = (lane >> 2) & 1;
+    *reinterpret_cast<uint4 *>(stg + lane * 32 + (sw << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+    *reinterpret_cast<uint4 *>(stg + lane * 32 + ((sw ^ 1) << 4)) = make_uint4(w[4], w[5], w[6], w[7]);
+    __syncwarp();
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const int piece = 32 * i + lane;
+        const int r = piece >> 1, half = piece & 1;
+        const int row = row0 + r, col = col0 + half * half_cols;
+        const uint4 val = *reinterpret_cast<const uint4 *>(stg + r * 32 + ((half ^ ((r >> 2) & 1)) << 4));
+        if (row < rows && col < cols)
+            *reinterpret_cast<uint4 *>(static_cast<char *>(out) + (static_cast<int64_t>(row) * ldo + col) * esize) = val;
+    }
+    __syncwarp();
 }
 
 template <int CG, int BN, bool MX, int KT>
@@ -394,6 +422,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int q = warp & 3;                          // TMEM lane quarter of this warp
         const int h = (warp - 2) >> 2;                   // which half of the tile's columns
         const uint32_t acc_empty0 = CG == 2 ? mapa_shared(bar_acc_empty, 0) : bar_acc_empty;
+        uint8_t *const stg_ptr = base_ptr + C::OFF_STG + (warp - 2) * kStgBytes;
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int u = pair; u < args.units; u += npairs) {
@@ -415,39 +444,35 @@ __global__ void __launch_bounds__(kThreads, 1)
                 else
                     mbar_arrive(bar_acc_empty + 8 * acc);
             }
-            const int ra = (ta * CG + static_cast<int>(rank)) * kBM + 32 * q + lane;   // slot-A row of this lane
+            const int row_base = (ta * CG + static_cast<int>(rank)) * kBM + 32 * q;   // this warp's first row
+            const int ra = row_base + lane;                                            // slot-A row of this lane
             const int col0 = tb * BN + h * C::COLS_WARP;                                // first slot-B row
-            if (ra < args.rows_a) {
+            if (args.mode == kEpiRows || ra < args.rows_a) {       // the row stores are warp-collective
                 if (args.mode == kEpiRows) {
-                    // D row ra, columns col0...: 16-byte stores (the row pitch is a
-                    // multiple of 16 bytes and N of 4 (fp32) or 8 (bf16) elements)
+                    // D rows of this warp in 32-byte column chunks through the staging
                     if (args.bf16) {
-                        uint4 *d = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(args.out) +
-                                                             static_cast<int64_t>(ra) * args.ldo + col0);
 #pragma unroll
-                        for (int c = 0; c < C::COLS_WARP / 8; ++c) {
-                            if (col0 + 8 * c < args.rows_b) {
-                                uint32_t w[4];
+                        for (int ch = 0; ch < C::COLS_WARP / 16; ++ch) {
+                            uint32_t w[8];
 #pragma unroll
-                                for (int i = 0; i < 4; ++i) {
-                                    __nv_bfloat162 p = __floats2bfloat162_rn(
-                                        __uint_as_float(v[8 * c + 2 * i]) * args.alpha,
-                                        __uint_as_float(v[8 * c + 2 * i + 1]) * args.alpha);
-                                    w[i] = *reinterpret_cast<uint32_t *>(&p);
-                                }
-                                d[c] = make_uint4(w[0], w[1], w[2], w[3]);
+                            for (int i = 0; i < 8; ++i) {
+                                __nv_bfloat162 p = __floats2bfloat162_rn(
+                                    __uint_as_float(v[16 * ch + 2 * i]) * args.alpha,
+                                    __uint_as_float(v[16 * ch + 2 * i + 1]) * args.alpha);
+                                w[i] = *reinterpret_cast<uint32_t *>(&p);
                             }
+                            store_chunk32(stg_ptr, w, args.out, args.ldo, 2, row_base, col0 + 16 * ch, 8, args.rows_a,
+                                          args.rows_b, lane);
                         }
                     } else {
-                        float4 *d = reinterpret_cast<float4 *>(static_cast<float *>(args.out) +
-                                                               static_cast<int64_t>(ra) * args.ldo + col0);
 #pragma unroll
-                        for (int c = 0; c < C::COLS_WARP / 4; ++c)
-                            if (col0 + 4 * c < args.rows_b)
-                                d[c] = make_float4(__uint_as_float(v[4 * c]) * args.alpha,
-                                                   __uint_as_float(v[4 * c + 1]) * args.alpha,
-                                                   __uint_as_float(v[4 * c + 2]) * args.alpha,
-                                                   __uint_as_float(v[4 * c + 3]) * args.alpha);
+                        for (int ch = 0; ch < C::COLS_WARP / 8; ++ch) {
+                            uint32_t w[8];
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) w[i] = __float_as_uint(__uint_as_float(v[8 * ch + i]) * args.alpha);
+                            store_chunk32(stg_ptr, w, args.out, args.ldo, 4, row_base, col0 + 8 * ch, 4, args.rows_a,
+                                          args.rows_b, lane);
+                        }
                     }
                 } else if (args.mode == kEpiSplitK) {
                     // fp32 partials, transposed: for a fixed column the 32 lanes of a
