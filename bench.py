@@ -159,7 +159,8 @@ def oracle_rows_tflops(inp, rows, nthreads=0):
 
 def cpu_sample_rows(inp, target_s):
     """Row sample whose oracle time is about target_s seconds (at least 1 row)."""
-    probe = np.arange(min(2, inp.M))
+    probe = np.arange(min(8, inp.M))
+    oracle_rows_tflops(inp, probe[:1])                 # first call: library load, thread start
     _, dt = oracle_rows_tflops(inp, probe)
     per_row = dt / len(probe)
     n = int(max(1, min(inp.M, target_s / max(per_row, 1e-9))))
@@ -178,8 +179,8 @@ def run_reference(args, inp):
     flops = 2.0 * len(rows) * inp.N * inp.K
     value = flops * len(times) / sum(times) / 1e12
     cores = os.cpu_count()
-    sample = "%d of %d rows of %s (all %d columns), fp64 C oracle, OpenMP" % (len(rows), inp.M, inp.name, inp.N,
-                                                                            cores)
+    sample = "%d of %d rows of %s (all %d columns), fp64 C oracle, OpenMP on %d cores" % (
+        len(rows), inp.M, inp.name, inp.N, cores)
     return {"metric": METRIC, "value": value, "unit": "TFLOP/s", "impl": "reference", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sum(times) / len(times),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
