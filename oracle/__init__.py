@@ -11,6 +11,9 @@ Functions (each follows the passage cited in ``oracle.c``):
 * ``gemm_pairs(inp, ii, jj)`` -> (D64, absdot) for sampled output elements.
 * ``round_bf16(x)`` -> uint16 bf16 bits (one rounding, ties to even).
 * ``scale_reorder(sf, rows, ksf)`` -> the 128x4 atom layout (uint8).
+* ``e2m1_encode(q)``, ``e4m3_encode(v)`` -> nearest code (ties to the even code).
+* ``quantize(X, fmt)`` -> (packed E2M1 codes, plain row-major scale bytes) of
+  fp32 or bf16 values, one scale per 16 (nvfp4) or 32 (mxfp4) values.
 
 Parity status of each function is recorded in the module docstrings of
 ``tests/test_oracle.py``; every function here is pinned there.
@@ -77,6 +80,13 @@ def _load():
         lib.oracle_scale_atom_bytes.restype = ctypes.c_int64
         lib.oracle_scale_reorder.argtypes = [_u8p, ctypes.c_int64, ctypes.c_int64, _u8p]
         lib.oracle_scale_reorder.restype = None
+        lib.oracle_e2m1_encode.argtypes = [ctypes.c_float]
+        lib.oracle_e2m1_encode.restype = ctypes.c_uint
+        lib.oracle_e4m3_encode.argtypes = [ctypes.c_float]
+        lib.oracle_e4m3_encode.restype = ctypes.c_uint
+        lib.oracle_quantize.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_int64,
+                                        ctypes.c_int, _u8p, _u8p]
+        lib.oracle_quantize.restype = ctypes.c_int
         _lib = lib
     return _lib
 
@@ -167,3 +177,27 @@ def scale_reorder(sf: np.ndarray, rows: int, ksf: int) -> np.ndarray:
     out = np.empty(scale_atom_bytes(rows, ksf), dtype=np.uint8)
     _load().oracle_scale_reorder(_ptr(sf, _u8p), rows, ksf, _ptr(out, _u8p))
     return out
+
+
+def e2m1_encode(q: float) -> int:
+    return int(_load().oracle_e2m1_encode(float(q)))
+
+
+def e4m3_encode(v: float) -> int:
+    return int(_load().oracle_e4m3_encode(float(v)))
+
+
+def quantize(X: np.ndarray, fmt: str) -> tuple[np.ndarray, np.ndarray]:
+    """X: [rows][K] float32 values, or uint16 bf16 bit patterns -> (codes [rows][K/2],
+    scales [rows][K/vec]) with vec 16 (nvfp4, E4M3) or 32 (mxfp4, E8M0)."""
+    X = np.ascontiguousarray(X)
+    assert X.ndim == 2 and X.dtype in (np.float32, np.uint16)
+    rows, K = X.shape
+    vec = 16 if fmt == "nvfp4" else 32
+    codes = np.empty((rows, K // 2), dtype=np.uint8)
+    sf = np.empty((rows, K // vec), dtype=np.uint8)
+    rc = _load().oracle_quantize(X.ctypes.data, int(X.dtype == np.uint16), rows, K, vec,
+                                 _ptr(codes, _u8p), _ptr(sf, _u8p))
+    if rc != 0:
+        raise ValueError("oracle_quantize rejected its arguments")
+    return codes, sf

@@ -1,5 +1,6 @@
 /*
- * oracle.c -- plain, slow, fp64 CPU oracle for the block-scaled FP4 GEMM.
+ * oracle.c -- plain, slow, fp64 CPU oracle for the block-scaled FP4 GEMM and
+ * for the quantisation step that feeds it (the latter decides in fp32).
  *
  * TEST INFRASTRUCTURE. Only the tests, the smoke check and the benchmark's
  * CPU-baseline leg may load this file's library. It shares no code, header,
@@ -221,4 +222,114 @@ void oracle_scale_reorder(const uint8_t *sf, int64_t rows, int64_t ksf, uint8_t 
             int64_t off = (r % 32) * 16 + ((r / 32) % 4) * 4 + (c % 4);
             out[atom * 512 + off] = sf[r * ksf + c];
         }
+}
+
+/* ---- online quantisation: values -> E2M1 codes + one scale per block ------ */
+/*
+ * The step before the GEMM: an activation row of K values becomes K E2M1
+ * codes packed two per byte (low nibble = even k) and one scale byte per
+ * block of vec values. The pages fix the formats and the block sizes
+ * ("[BUG] Add FP4 TMA kernel example for Blackwell in CuTe Python DSL",
+ * "Scale Factor Granularity" and "Code Reference": Float8E4M3FN scales, one per
+ * 16 values; "TMA Pipelines, Tensor Cores, and ctm-rs Interop", section 1:
+ * Float8E8M0FNU scales for MXFP4) but not how a scale is chosen. The reading
+ * taken here:
+ *   NVFP4: s = E4M3(amax / 6), the division in fp32, then round to nearest
+ *          E4M3 (ties to the even code, saturating at 448);
+ *   MXFP4: s = 2^(floor(log2 amax) - 2), exponent clamped to [-127, 127]; an
+ *          all-zero block gets 2^-127 (byte 0);
+ *   code = E2M1 value nearest to q = x / s, with q rounded to fp32 first; ties
+ *          to the even code; |q| >= 6 saturates to 6; the sign bit of x is
+ *          kept (so -0 and negatives that round to 0 give code 8). An NVFP4
+ *          block whose scale is 0 gets all codes 0.
+ * Every decision above is taken in fp32, the precision the kernel works in.
+ */
+
+/* Nearest E2M1 code to q: search the eight magnitudes, a tie keeps the even code. */
+unsigned oracle_e2m1_encode(float q)
+{
+    const unsigned sign = signbit(q) ? 8u : 0u;
+    const double a = fabs((double)q);
+    if (a >= 6.0) return sign | 7u;
+    unsigned best = 0;
+    for (unsigned c = 1; c < 8; ++c) {
+        const double dc = fabs(a - oracle_e2m1(c)), db = fabs(a - oracle_e2m1(best));
+        if (dc < db || (dc == db && c % 2 == 0)) best = c;
+    }
+    return sign | best;
+}
+
+/* Nearest E4M3 code to v >= 0 among the finite non-negative codes 0x00..0x7E
+ * (a tie keeps the even code); v >= 448 saturates to 448 (0x7E). */
+unsigned oracle_e4m3_encode(float v)
+{
+    if (v >= 448.0f) return 0x7Eu;
+    unsigned best = 0;
+    for (unsigned c = 1; c <= 0x7Eu; ++c) {
+        const double dc = fabs((double)v - oracle_e4m3(c)), db = fabs((double)v - oracle_e4m3(best));
+        if (dc < db || (dc == db && c % 2 == 0)) best = c;
+    }
+    return best;
+}
+
+/* One input value as fp32: bf16 bits widen exactly (they are fp32's top half). */
+static float load_value(const void *X, int in_bf16, int64_t idx)
+{
+    if (!in_bf16) return ((const float *)X)[idx];
+    uint32_t u = (uint32_t)((const uint16_t *)X)[idx] << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return f;
+}
+
+/*
+ * X: rows x K values (fp32, or bf16 bits when in_bf16), row-major.
+ * codes: rows x K/2 bytes; sf: rows x K/vec scale bytes, plain row-major.
+ * Returns 0, or -1 on a bad argument. Non-finite inputs are outside the
+ * definition.
+ */
+int oracle_quantize(const void *X, int in_bf16, int64_t rows, int64_t K, int vec, uint8_t *codes, uint8_t *sf)
+{
+    if (vec != 16 && vec != 32) return -1;
+    if (rows < 0 || K < 0 || K % vec != 0) return -1;
+    const int64_t nb = K / vec;
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; ++r) {
+        for (int64_t b = 0; b < nb; ++b) {
+            float x[32];
+            float amax = 0.0f;
+            for (int i = 0; i < vec; ++i) {
+                x[i] = load_value(X, in_bf16, r * K + b * vec + i);
+                amax = fmaxf(amax, fabsf(x[i]));
+            }
+            unsigned scode;
+            float s;
+            if (vec == 16) {
+                const float t = amax / 6.0f;
+                scode = oracle_e4m3_encode(t);
+                s = (float)oracle_e4m3(scode);
+            } else {
+                int e2 = -127;
+                if (amax > 0.0f) {
+                    int e;
+                    (void)frexpf(amax, &e);          /* amax = f * 2^e, f in [0.5, 1) */
+                    e2 = (e - 1) - 2;
+                    if (e2 < -127) e2 = -127;
+                    if (e2 > 127) e2 = 127;
+                }
+                scode = (unsigned)(e2 + 127);
+                s = ldexpf(1.0f, e2);
+            }
+            sf[r * nb + b] = (uint8_t)scode;
+            for (int i = 0; i < vec; i += 2) {
+                unsigned lo = 0, hi = 0;
+                if (s != 0.0f) {
+                    lo = oracle_e2m1_encode(x[i] / s);
+                    hi = oracle_e2m1_encode(x[i + 1] / s);
+                }
+                codes[r * (K / 2) + (b * vec + i) / 2] = (uint8_t)(lo | (hi << 4));
+            }
+        }
+    }
+    return 0;
 }

@@ -1,8 +1,9 @@
 """Pin strength: plausible mistakes planted in copies of the oracle must fail a pin.
 
 Each case edits one line of oracle.c in a temporary copy (on the CPU), builds
-it, and runs tests/test_oracle.py against that library in a child process.
-The pins must reject every mutant.
+it, and runs the pins of the part it touches (tests/test_oracle.py for the
+GEMM, tests/test_oracle_quant.py for the quantiser) against that library in a
+child process. The pins must reject every mutant.
 """
 from __future__ import annotations
 
@@ -36,12 +37,28 @@ MUTANTS = {
     "reorder_atoms_row_major_by_k": ("(r / 128) * kc4 + c / 4", "(c / 4) * ((rows + 127) / 128) + r / 128"),
 }
 
+QUANT_MUTANTS = {
+    "e2m1_ties_to_odd": ("if (dc < db || (dc == db && c % 2 == 0)) best = c;\n    }\n    return sign | best;",
+                         "if (dc < db || (dc == db && c % 2 == 1)) best = c;\n    }\n    return sign | best;"),
+    "e2m1_sign_dropped": ("const unsigned sign = signbit(q) ? 8u : 0u;", "const unsigned sign = 0u;"),
+    "e2m1_no_saturation": ("if (a >= 6.0) return sign | 7u;", "if (a >= 6.0) return sign | 6u;"),
+    "e4m3_ties_up": ("if (dc < db || (dc == db && c % 2 == 0)) best = c;\n    }\n    return best;",
+                     "if (dc <= db) best = c;\n    }\n    return best;"),
+    "e4m3_saturates_to_nan": ("if (v >= 448.0f) return 0x7Eu;", "if (v >= 448.0f) return 0x7Fu;"),
+    "nv_scale_amax_over_4": ("const float t = amax / 6.0f;", "const float t = amax / 4.0f;"),
+    "mx_exponent_off_by_one": ("e2 = (e - 1) - 2;", "e2 = (e - 1) - 1;"),
+    "mx_zero_block_scale": ("int e2 = -127;", "int e2 = 0;"),
+    "nibbles_swapped": ("(uint8_t)(lo | (hi << 4))", "(uint8_t)(hi | (lo << 4))"),
+    "zero_scale_keeps_sign": ("if (s != 0.0f) {", "if (1) {"),
+    "bf16_widened_wrong": ("uint32_t u = (uint32_t)((const uint16_t *)X)[idx] << 16;",
+                           "uint32_t u = (uint32_t)((const uint16_t *)X)[idx] << 15;"),
+    "block_stride_wrong": ("load_value(X, in_bf16, r * K + b * vec + i)", "load_value(X, in_bf16, r * K + b * 16 + i)"),
+}
 
-@pytest.mark.parametrize("name", sorted(MUTANTS))
-def test_pins_reject_mutant(name, tmp_path):
-    old, new = MUTANTS[name]
+
+def _run_mutant(old, new, pins, tmp_path):
     src = open(SRC).read()
-    assert src.count(old) == 1, "mutation site not found: %s" % name
+    assert src.count(old) == 1, "mutation site not found: %r" % old
     mutated = tmp_path / "oracle.c"
     mutated.write_text(src.replace(old, new))
     lib = tmp_path / "mutant.so"
@@ -49,6 +66,18 @@ def test_pins_reject_mutant(name, tmp_path):
                     str(mutated), "-o", str(lib), "-lm"], check=True)
     env = dict(os.environ, FP4_ORACLE_LIB=str(lib))
     r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-p", "no:cacheprovider",
-                        os.path.join(ROOT, "tests", "test_oracle.py")],
+                        os.path.join(ROOT, "tests", pins)],
                        cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
+    return r
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_reject_mutant(name, tmp_path):
+    r = _run_mutant(*MUTANTS[name], "test_oracle.py", tmp_path)
+    assert r.returncode != 0, "mutant %s survived the pins:\n%s" % (name, r.stdout[-2000:])
+
+
+@pytest.mark.parametrize("name", sorted(QUANT_MUTANTS))
+def test_quantiser_pins_reject_mutant(name, tmp_path):
+    r = _run_mutant(*QUANT_MUTANTS[name], "test_oracle_quant.py", tmp_path)
     assert r.returncode != 0, "mutant %s survived the pins:\n%s" % (name, r.stdout[-2000:])
