@@ -23,6 +23,12 @@ own GPU with no collective in the data path (weak scaling).
 
 --impl reference times the CPU oracle (the only reference this project has)
 on the same workload, one bounded row sample per step.
+
+--op quantize measures the quantisation step that feeds the GEMM instead
+(fp4_quantize: bf16 or fp32 activations -> E2M1 codes + atom-layout scales),
+against the HBM roofline: its bytes (values read, codes and scale atoms
+written) over its CUDA-event duration, with the CPU oracle's quantiser on a
+row sample as the cpu_baseline. Its workloads are the quant_* names.
 """
 from __future__ import annotations
 
@@ -331,13 +337,128 @@ def run_ours(args, inp, rank, ws, local):
     return result
 
 
+QUANT_METRIC = "FP4 activation quantisation GB/s on 1 GB300 and % of HBM bandwidth"
+DEFAULT_QUANT_WORKLOAD = "quant_nvfp4_8192x4096_bf16"
+
+
+def quant_bytes(rows, K, vec, in_bytes, atom_bytes):
+    return rows * K * in_bytes + rows * K // 2 + atom_bytes
+
+
+def run_quant(args, rank, ws, local):
+    """Times fp4_quantize (atom-layout scales) on a named activation workload."""
+    import torch
+    import block_scaled_fp4_sfa_gb300 as fp4
+    name = args.workload if args.workload in W.QUANT_WORKLOADS else DEFAULT_QUANT_WORKLOAD
+    fmt, X = W.make_quant_workload(name, seed=rank)
+    rows, K = X.shape
+    vec = 16 if fmt == "nvfp4" else 32
+    in_dtype = "bf16" if X.dtype == np.uint16 else "f32"
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    fp4.load()
+    stream = torch.cuda.current_stream()
+    s = stream.cuda_stream
+    hX = torch.from_numpy(X.view(np.int16) if X.dtype == np.uint16 else X)
+    Xd = hX.to(dev)
+    atom_bytes = fp4.scale_atom_bytes(rows, K, vec)
+    codes = torch.empty(rows * K // 2, dtype=torch.uint8, device=dev)
+    sf = torch.empty(atom_bytes, dtype=torch.uint8, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    nbytes = quant_bytes(rows, K, vec, X.itemsize, atom_bytes)
+
+    def step():
+        fp4.quantize(fmt, Xd, rows, K, codes, sf, in_dtype=in_dtype, layout="atom", stream=s)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        torch.cuda._sleep(SPACER_CYCLES)
+        step()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local if not args.quick else -1) as clk:
+        time.sleep(0.2)
+        for e0, e1 in ev:
+            flush.zero_()
+            torch.cuda._sleep(SPACER_CYCLES)
+            e0.record(stream)
+            step()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        if ws > 1:
+            torch.distributed.barrier()
+    st = fp4.get_device_status(s)
+    if st != 0:
+        raise RuntimeError("device status after timing: %s" % fp4.status_string(st))
+    ms = [a.elapsed_time(b) for a, b in ev]
+    total_ms = slowest_rank_ms(sum(ms), ws, dev)
+    ms_per_step = total_ms / args.steps
+    value = nbytes * args.steps * ws / (total_ms * 1e-3) / 1e9
+    cfg = {"workload": name, "format": fmt, "rows": rows, "K": K, "in": in_dtype, "scales": "atom",
+           "l2": "flushed between steps (256 MiB write, outside the step events)",
+           "parallelism": "replicas" if ws > 1 else "single"}
+    res = {"metric": QUANT_METRIC, "value": value, "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
+           "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+           "vs_baseline": None, "dtype": in_dtype + "->e2m1", "data": "synthetic", "config": cfg}
+    if args.quick:
+        return res
+    # e2e: pinned host values in, codes and scales back to pinned host memory
+    pX = hX.pin_memory()
+    pc = torch.empty(rows * K // 2, dtype=torch.uint8).pin_memory()
+    ps = torch.empty(atom_bytes, dtype=torch.uint8).pin_memory()
+    e_steps = max(3, min(args.steps, 20))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(e_steps):
+        Xd.copy_(pX, non_blocking=True)
+        step()
+        pc.copy_(codes, non_blocking=True)
+        ps.copy_(sf, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e_steps
+    _, hbm_peak, peak_src = peaks()
+    avg_ms = sum(ms) / len(ms)
+    achieved = nbytes / (avg_ms * 1e-3) / 1e9
+    res.update({
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                     "frac": achieved / hbm_peak, "traffic": None,
+                     "peak_source": "%s HBM copy bandwidth" % peak_src, "kernel": "quantize_kernel",
+                     "kernel_us": 1e3 * avg_ms, "algorithmic_bytes": nbytes},
+        "e2e": {"value": nbytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+                "h2d_bytes_per_step": hX.numel() * hX.element_size(), "d2h_bytes_per_step": pc.numel() + ps.numel()},
+        "gpu_launches": args.steps,
+        "clocks": clk.summary(),
+    })
+    if rank == 0 and not args.no_cpu_baseline:
+        import oracle
+        n = 64
+        t0 = time.perf_counter()
+        oracle.quantize(X[:n], fmt)
+        dt = time.perf_counter() - t0
+        n = int(max(1, min(rows, n * args.cpu_sample_s / 4 / max(dt, 1e-6))))
+        t0 = time.perf_counter()
+        oracle.quantize(X[:n], fmt)
+        dt = time.perf_counter() - t0
+        res["cpu_baseline"] = {"value": quant_bytes(n, K, vec, X.itemsize, 0) / dt / 1e9, "unit": "GB/s",
+                               "cores": os.cpu_count(), "kind": "oracle",
+                               "sample": "first %d of %d rows of %s, %.1f s, C oracle (fp32 decisions), plain scales"
+                                         % (n, rows, name, dt)}
+    return res
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=W.config_names())
+    ap.add_argument("--op", choices=["gemm", "quantize"], default="gemm")
+    ap.add_argument("--workload", default=None, choices=W.config_names() + sorted(W.QUANT_WORKLOADS))
     ap.add_argument("--cpu-sample-s", type=float, default=12.0, help="oracle seconds for cpu_baseline")
     ap.add_argument("--ref-step-s", type=float, default=3.0, help="oracle seconds per reference step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -348,8 +469,23 @@ def main():
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     ws, rank, local = dist_env()
+    if args.workload is None:
+        args.workload = DEFAULT_QUANT_WORKLOAD if args.op == "quantize" else DEFAULT_WORKLOAD
+    if (args.op == "quantize") != (args.workload in W.QUANT_WORKLOADS):
+        ap.error("--op %s does not take workload %s" % (args.op, args.workload))
 
-    if args.impl == "reference":
+    if args.op == "quantize":
+        if args.impl == "reference":
+            ap.error("--impl reference times the GEMM's oracle; use --op gemm")
+        if ws > 1:
+            import torch
+            torch.cuda.set_device(local)
+            torch.distributed.init_process_group("nccl")
+        res = run_quant(args, rank, ws, local)
+        if ws > 1:
+            import torch
+            torch.distributed.destroy_process_group()
+    elif args.impl == "reference":
         if rank != 0:
             return
         inp = W.make_config(args.workload)

@@ -1,7 +1,8 @@
 """Python binding of the GB300 block-scaled FP4 GEMM library (libfp4gemm.so).
 
-Argument marshalling only: every step of the GEMM runs in the library's CUDA
-kernels, behind the C ABI declared in include/fp4_gemm.h. Buffers may be torch
+Argument marshalling only: every step of the GEMM and of the quantisation that
+feeds it runs in the library's CUDA kernels, behind the C ABI declared in
+include/fp4_gemm.h and include/fp4_quant.h. Buffers may be torch
 tensors (device pointers taken with ``data_ptr()``), numpy arrays (host
 pointers, for ``gemm_host``) or raw integer addresses. ``stream`` is a
 ``torch.cuda.Stream``, a raw ``cudaStream_t`` integer, or None for torch's
@@ -19,7 +20,7 @@ from . import _build
 __all__ = ["FP4_OK", "Fp4Error", "load", "build", "gemm", "gemm_nvfp4", "gemm_mxfp4", "gemm_nvfp4_prepacked",
            "gemm_mxfp4_prepacked", "gemm_host", "scale_reorder", "scale_atom_bytes", "get_device_status",
            "status_string", "set_wait_limit_ms", "GemmConfig", "FMT", "OUT", "gemm_static_scratch",
-           "STATIC_SCRATCH_BYTES"]
+           "STATIC_SCRATCH_BYTES", "quantize", "IN", "SF_LAYOUT"]
 
 FP4_OK = 0
 STATUS_NAMES = {0: "FP4_OK", 1: "FP4_ERR_INVALID_ARG", 2: "FP4_ERR_UNSUPPORTED", 3: "FP4_ERR_MISALIGNED",
@@ -27,6 +28,8 @@ STATUS_NAMES = {0: "FP4_OK", 1: "FP4_ERR_INVALID_ARG", 2: "FP4_ERR_UNSUPPORTED",
 STATIC_SCRATCH_BYTES = 16 << 20
 FMT = {"nvfp4": 0, "mxfp4": 1}
 OUT = {"f32": 0, "bf16": 1}
+IN = {"f32": 0, "bf16": 1}
+SF_LAYOUT = {"plain": 0, "atom": 1}
 
 _lib = None
 
@@ -78,6 +81,8 @@ def load():
     lib.fp4_status_string.restype = ctypes.c_char_p
     lib.fp4_set_wait_limit_ms.argtypes = [i64]
     lib.fp4_set_wait_limit_ms.restype = None
+    lib.fp4_quantize.argtypes = [i32, vp, i32, i64, i64, vp, vp, i32, vp]
+    lib.fp4_quantize.restype = i32
     _lib = lib
     return lib
 
@@ -169,6 +174,17 @@ def scale_reorder(sf, sf_atom, rows: int, k: int, vec: int, stream=None, check: 
     st = load().fp4_scale_reorder(_ptr(sf), _ptr(sf_atom), int(rows), int(k), int(vec), _stream(stream))
     if check:
         _check(st, "fp4_scale_reorder")
+    return st
+
+
+def quantize(fmt: str, X, rows: int, K: int, codes, sf, *, in_dtype: str = "bf16", layout: str = "plain",
+             stream=None, check: bool = True) -> int:
+    """fp4_quantize: X [rows][K] (fp32 or bf16) -> E2M1 codes [rows][K/2] and scale bytes
+    (plain [rows][K/vec], or the 128x4 atom layout for the prepacked GEMM calls)."""
+    st = load().fp4_quantize(FMT[fmt], _ptr(X), IN[in_dtype], int(rows), int(K), _ptr(codes), _ptr(sf),
+                             SF_LAYOUT[layout], _stream(stream))
+    if check:
+        _check(st, "fp4_quantize")
     return st
 
 

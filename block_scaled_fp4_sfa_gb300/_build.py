@@ -1,8 +1,9 @@
 """Builds the CUDA library (libfp4gemm.so) in-tree with nvcc for sm_103a.
 
-One translation unit, one -gencode; the static CUDA runtime is linked in and
-the driver's tensor-map encoder is looked up at run time, so the library needs
-no -lcuda.
+Two translation units (the GEMM and the quantiser) compiled in parallel, one
+-gencode, then linked into one shared library; the static CUDA runtime is
+linked in and the driver's tensor-map encoder is looked up at run time, so the
+library needs no -lcuda.
 """
 from __future__ import annotations
 
@@ -15,8 +16,9 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libfp4gemm.so")
-SOURCES = [os.path.join(CSRC, "fp4_gemm.cu")]
-DEPS = SOURCES + [os.path.join(CSRC, "ptx.cuh"), os.path.join(INCLUDE, "fp4_gemm.h")]
+SOURCES = [os.path.join(CSRC, "fp4_gemm.cu"), os.path.join(CSRC, "fp4_quant.cu")]
+DEPS = SOURCES + [os.path.join(CSRC, "ptx.cuh"), os.path.join(INCLUDE, "fp4_gemm.h"),
+                  os.path.join(INCLUDE, "fp4_quant.h")]
 
 ARCH = "-gencode=arch=compute_103a,code=sm_103a"
 
@@ -43,10 +45,22 @@ def build(force: bool = False, verbose: bool = False, extra=()) -> str:
     if not force and up_to_date() and not extra:
         return LIB
     tmp = LIB + ".tmp%d" % os.getpid()
-    cmd = [nvcc(), *flags(extra), "-shared", "-o", tmp, *SOURCES]
-    if verbose:
-        print(" ".join(cmd), file=sys.stderr)
-    subprocess.run(cmd, check=True)
+    objs = [tmp + ".%d.o" % i for i in range(len(SOURCES))]
+    procs = []
+    for src, obj in zip(SOURCES, objs):
+        cmd = [nvcc(), *flags(extra), "-c", "-o", obj, src]
+        if verbose:
+            print(" ".join(cmd), file=sys.stderr)
+        procs.append((cmd, subprocess.Popen(cmd)))
+    failed = [cmd for cmd, p in procs if p.wait() != 0]
+    try:
+        if failed:
+            raise subprocess.CalledProcessError(1, failed[0])
+        subprocess.run([nvcc(), ARCH, "-shared", "-o", tmp, *objs], check=True)
+    finally:
+        for obj in objs:
+            if os.path.exists(obj):
+                os.remove(obj)
     os.replace(tmp, LIB)
     return LIB
 

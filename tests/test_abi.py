@@ -11,7 +11,7 @@ import numpy as np
 import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-HEADER = os.path.join(ROOT, "include", "fp4_gemm.h")
+HEADERS = [os.path.join(ROOT, "include", h) for h in ("fp4_gemm.h", "fp4_quant.h")]
 
 
 @pytest.fixture(scope="module")
@@ -22,7 +22,7 @@ def fp4():
 
 
 def declared_functions():
-    text = open(HEADER).read()
+    text = "".join(open(h).read() for h in HEADERS)
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
     return sorted(set(re.findall(r"\b(fp4_[a-z0-9_]+)\s*\(", text)))
 
@@ -30,7 +30,8 @@ def declared_functions():
 def test_header_declares_the_boundary():
     names = declared_functions()
     for must in ("fp4_gemm_nvfp4", "fp4_gemm_mxfp4", "fp4_gemm_nvfp4_prepacked", "fp4_gemm_mxfp4_prepacked",
-                 "fp4_scale_atom_bytes", "fp4_scale_reorder", "fp4_get_device_status", "fp4_status_string"):
+                 "fp4_scale_atom_bytes", "fp4_scale_reorder", "fp4_get_device_status", "fp4_status_string",
+                 "fp4_quantize"):
         assert must in names
 
 
@@ -95,6 +96,27 @@ def test_host_validation_without_device(fp4):
     assert lib.fp4_scale_reorder(p, p + 4, 10, 64, 16, 0) == 3
     assert lib.fp4_scale_reorder(p, p, 0, 64, 16, 0) == 0
     assert lib.fp4_gemm_host(0, p, p, p, p, 1.0, p, 64, 64, 40, 0, 0) == 2
+
+
+def test_quantize_host_validation_without_device(fp4):
+    buf = np.zeros(4096 + 16, np.uint8)
+    p = buf.ctypes.data + (-buf.ctypes.data) % 16
+    q = fp4.load().fp4_quantize
+    # no-ops
+    assert q(0, p, 1, 0, 64, p, p, 0, 0) == 0
+    assert q(0, p, 1, 8, 0, p, p, 1, 0) == 0
+    # enums, sizes, pointers, alignment
+    assert q(2, p, 1, 8, 64, p, p, 0, 0) == 1
+    assert q(0, p, 2, 8, 64, p, p, 0, 0) == 1
+    assert q(0, p, 1, 8, 64, p, p, 2, 0) == 1
+    assert q(0, p, 1, -1, 64, p, p, 0, 0) == 1
+    assert q(0, p, 1, 8, 48, p, p, 0, 0) == 2            # K % 32 != 0
+    assert q(0, None, 1, 8, 64, p, p, 0, 0) == 1
+    assert q(1, p, 1, 8, 64, p, None, 0, 0) == 1
+    assert q(0, p + 2, 1, 8, 64, p, p, 0, 0) == 3        # X not 16-byte aligned
+    assert q(0, p, 1, 8, 64, p + 8, p, 0, 0) == 3        # codes not 16-byte aligned
+    assert q(0, p, 1, 8, 64, p, p + 4, 1, 0) == 3        # atom scales not 16-byte aligned
+    assert q(0, p, 1, 1 << 40, 64, p, p, 0, 0) == 2      # beyond the index range
 
 
 def test_python_binding_raises(fp4):

@@ -229,3 +229,45 @@ def make_config(name: str, seed: int = 0) -> GemmInputs:
     if name in ("nvfp4_8191x3000x5120_f32", "nvfp4_1x28672x4096_f32"):
         return make_random(fmt, M, N, K, dist="t3", alpha=alpha, out=out, seed=seed, name=name)
     return make_random(fmt, M, N, K, dist="normal", alpha=alpha, out=out, seed=seed, name=name)
+
+
+# ---- raw values for the quantisation step -------------------------------------
+#
+# The quantiser's inputs are plain activations: seeded draws rounded to the
+# input dtype (bf16 through torch's float32 -> bfloat16 cast, round to nearest
+# even). Nothing here quantises them.
+
+QUANT_WORKLOADS = {
+    # the A-side activations of the 8192 x 14336 x 4096 and 8192 x 4096 x 14336
+    # projections, and of the 8192^3 MXFP4 GEMM
+    "quant_nvfp4_8192x4096_bf16": dict(fmt="nvfp4", rows=8192, K=4096, dtype="bf16"),
+    "quant_nvfp4_8192x14336_bf16": dict(fmt="nvfp4", rows=8192, K=14336, dtype="bf16"),
+    "quant_mxfp4_8192x8192_bf16": dict(fmt="mxfp4", rows=8192, K=8192, dtype="bf16"),
+    "quant_nvfp4_8192x4096_f32": dict(fmt="nvfp4", rows=8192, K=4096, dtype="f32"),
+}
+
+
+def to_bf16_bits(x32: np.ndarray) -> np.ndarray:
+    """float32 -> bf16 bit patterns (uint16), round to nearest even (torch's cast)."""
+    import torch
+    t = torch.from_numpy(np.ascontiguousarray(x32, dtype=np.float32)).to(torch.bfloat16)
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+def make_values(rows: int, K: int, *, dist: str = "normal", std: float = 1.0, dtype: str = "bf16",
+                seed: int = 0) -> np.ndarray:
+    """rows x K activations: float32 values, or uint16 bf16 bit patterns for dtype "bf16"."""
+    rng = np.random.default_rng(2 * seed)
+    if dist == "normal":
+        x = rng.standard_normal((rows, K), dtype=np.float32) * np.float32(std)
+    elif dist == "t3":
+        x = (rng.standard_t(3, (rows, K)) * std).astype(np.float32)
+    else:
+        raise ValueError(dist)
+    return x if dtype == "f32" else to_bf16_bits(x)
+
+
+def make_quant_workload(name: str, seed: int = 0):
+    """(fmt, X) of a named quantisation workload."""
+    w = QUANT_WORKLOADS[name]
+    return w["fmt"], make_values(w["rows"], w["K"], dtype=w["dtype"], seed=seed)
