@@ -70,7 +70,8 @@ constexpr int kBK = 256;          // FP4 elements per k-tile
 constexpr int kBKBytes = 128;     // bytes per row per k-tile
 constexpr int kAtomBytes = 512;   // one 128-row x 4-column scale atom
 constexpr int kEpiWarps = 8;
-constexpr int kThreads = 64 + 32 * kEpiWarps;   // producer warp, MMA warp, epilogue warps
+constexpr int kWaiterWarp = 2 + kEpiWarps;
+constexpr int kThreads = 32 * (kWaiterWarp + 1);   // producer, MMA, epilogue warps, waiter warp
 constexpr int kStgBytes = 32 * 32;              // per-warp store staging: 32 rows x 32 bytes
 constexpr int kSmemLimit = 232448;
 
@@ -166,6 +167,53 @@ __device__ __forceinline__ bool wait(uint32_t bar, uint32_t parity, uint64_t lim
     return wait_slow(bar, parity, limit_ns, abort_flag);
 }
 
+// Acquire-wait (cluster scope) for barriers that the peer CTA of a pair arrives on.
+__device__ __noinline__ bool wait_cluster_slow(uint32_t bar, uint32_t parity, uint64_t limit_ns,
+                                               volatile uint32_t *abort_flag)
+{
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait_cluster(bar, parity)) return true;
+        if ((it & 255u) == 0) {
+            if (*abort_flag != 0) return false;
+            if (global_timer_ns() - t0 > limit_ns) {
+                record_error(FP4_ERR_TIMEOUT);
+                *abort_flag = 1;
+                return false;
+            }
+        }
+    }
+}
+
+__device__ __forceinline__ bool wait_cluster(uint32_t bar, uint32_t parity, uint64_t limit_ns,
+                                             volatile uint32_t *abort_flag)
+{
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    return wait_cluster_slow(bar, parity, limit_ns, abort_flag);
+}
+
+// MMA thread: waits (bounded) until the waiter's count passes `consumed` and
+// returns it (0 when the wait gave up); the count read with acquire semantics
+// orders the stage's landing (and the accumulator's draining) before the MMAs
+// that follow.
+__device__ __noinline__ uint32_t take_credit(uint32_t ready_addr, uint32_t consumed, uint64_t limit_ns,
+                                             volatile uint32_t *abort_flag)
+{
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t it = 1;; ++it) {
+        const uint32_t ready = ld_acquire_shared(ready_addr);
+        if (ready > consumed) return ready;
+        if ((it & 63u) == 0) {
+            if (*abort_flag != 0) return 0;
+            if (global_timer_ns() - t0 > limit_ns) {
+                record_error(FP4_ERR_TIMEOUT);
+                *abort_flag = 1;
+                return 0;
+            }
+        }
+    }
+}
+
 // Unit u -> (slot-A tile, slot-B tile, split). Splits are outermost; inside a
 // split, tiles go in groups of `group_b` slot-B tiles with slot-A tiles
 // running across each group, so the CTAs in flight share operand rows in L2.
@@ -248,6 +296,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t *const tmem_holder = reinterpret_cast<uint32_t *>(base_ptr + C::OFF_BAR + 16 * C::STAGES + 40);
     volatile uint32_t *const abort_flag =
         reinterpret_cast<volatile uint32_t *>(base_ptr + C::OFF_BAR + 16 * C::STAGES + 44);
+    // stages the waiter warp has seen land (a count, in the MMA issue order)
+    const uint32_t ready_addr = base + C::OFF_BAR + 16 * C::STAGES + 48;
 
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
@@ -266,6 +316,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mbar_init(bar_drain, 1);
         *abort_flag = 0;
+        st_release_shared(ready_addr, 0);
         fence_mbarrier_init();
     }
     if (threadIdx.x == 32) {
@@ -354,22 +405,24 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t desc_sfa0 = smem_desc(base + C::OFF_SFA, 0, 128, 0);
             const uint64_t desc_sfb0 = smem_desc(base + C::OFF_SFB, 0, 128, 0);
             int stage = 0;
-            uint32_t phase = 0;
             int acc = 0;
-            uint32_t acc_phase = 0;
+            uint32_t consumed = 0, ready = 0;    // stages issued / stages known to have landed
             bool ok = true;
             for (int u = pair; ok && u < args.units; u += npairs) {
                 int ta, tb, split;
                 unit_coords(args, u, ta, tb, split);
                 const int kt0 = split * args.kps;
                 const int kt1 = min(kt0 + args.kps, args.k_tiles);
-                if (!wait(bar_acc_empty + 8 * acc, acc_phase ^ 1u, args.wait_ns, abort_flag)) break;
-                tc_fence_after();
                 const uint32_t d_tmem = tmem + static_cast<uint32_t>(acc * BN);
                 for (int kt = kt0; kt < kt1; kt += KT) {
-                    if (!wait(bar_full + 8 * stage, phase, args.wait_ns, abort_flag)) {
-                        ok = false;
-                        break;
+                    // The waiter warp has seen this stage land (and, for a unit's first
+                    // stage, the accumulator drained) once its count passes `consumed`.
+                    if (ready == consumed) {
+                        ready = take_credit(ready_addr, consumed, args.wait_ns, abort_flag);
+                        if (ready == 0) {
+                            ok = false;
+                            break;
+                        }
                     }
                     tc_fence_after();
 #pragma unroll
@@ -399,13 +452,48 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                     }
                     tc_commit<CG>(bar_empty + 8 * stage);
+                    ++consumed;
+                    if (++stage == C::STAGES) stage = 0;
+                }
+                if (!ok) break;
+                tc_commit<CG>(bar_acc_full + 8 * acc);
+                if (C::ACC_BUFS == 2) acc ^= 1;
+            }
+            // Every MMA and scale copy this thread issued completes before teardown.
+            tc_commit<CG>(bar_drain, 1);
+            wait(bar_drain, 0, args.wait_ns, abort_flag);
+        }
+    } else if (warp == kWaiterWarp) {
+        // ------------------------------------------------------------ waiter
+        // Waits, in the MMA issue order, for each unit's accumulator to be
+        // drained and for each stage to land, and publishes the running count.
+        // The MMA thread then never blocks in an mbarrier wait: on this part a
+        // wait in the issuing thread costs about 200 cycles in which the tensor
+        // core runs dry.
+        if (lane == 0 && rank == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            int acc = 0;
+            uint32_t acc_phase = 0;
+            uint32_t seen = 0;
+            bool ok = true;
+            for (int u = pair; ok && u < args.units; u += npairs) {
+                int ta, tb, split;
+                unit_coords(args, u, ta, tb, split);
+                const int kt0 = split * args.kps;
+                const int kt1 = min(kt0 + args.kps, args.k_tiles);
+                if (!wait_cluster(bar_acc_empty + 8 * acc, acc_phase ^ 1u, args.wait_ns, abort_flag)) break;
+                for (int kt = kt0; kt < kt1; kt += KT) {
+                    if (!wait(bar_full + 8 * stage, phase, args.wait_ns, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    st_release_shared(ready_addr, ++seen);
                     if (++stage == C::STAGES) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
-                if (!ok) break;
-                tc_commit<CG>(bar_acc_full + 8 * acc);
                 if (C::ACC_BUFS == 2) {
                     acc ^= 1;
                     if (acc == 0) acc_phase ^= 1u;
@@ -413,9 +501,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     acc_phase ^= 1u;
                 }
             }
-            // Every MMA and scale copy this thread issued completes before teardown.
-            tc_commit<CG>(bar_drain, 1);
-            wait(bar_drain, 0, args.wait_ns, abort_flag);
         }
     } else {
         // ------------------------------------------------------------ epilogue
@@ -435,7 +520,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_load_cols<C::COLS_WARP>(tmem + (static_cast<uint32_t>(32 * q) << 16) +
                                              static_cast<uint32_t>(acc * BN + h * C::COLS_WARP),
                                          v);
-            tmem_ld_wait();
+            tmem_ld_wait_regs(v);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) {
@@ -840,11 +925,17 @@ fp4_status make_plan(int64_t M, int64_t N, int64_t K, bool rows_ok, bool mx, int
     if (splits == 0) {
         splits = 1;
         if (p.swap && tiles < slots) {
-            // minimise (waves x k-tiles per split), preferring fewer splits on ties
+            // Estimated cycles: waves of units x (k-tiles x per-k-tile issue time +
+            // per-unit epilogue), plus, when split, the fp32 partials written and
+            // read again and the reduce kernel's launch. Fewer splits win ties.
+            constexpr double kTileCycles = 700.0, kUnitCycles = 1500.0, kReduceCycles = 10000.0;
+            constexpr double kBytesPerCycle = 3000.0;      // HBM bytes per SM-clock cycle, whole GPU
             double best = 1e30;
             for (int s = 1; s <= std::min<int64_t>(k_tiles, 16); ++s) {
                 const double waves = static_cast<double>(cdiv(tiles * s, slots));
-                const double cost = waves * static_cast<double>(cdiv(k_tiles, s)) * (1.0 + 0.02 * (s - 1));
+                double cost = waves * (static_cast<double>(cdiv(k_tiles, s)) * kTileCycles + kUnitCycles);
+                if (s > 1)
+                    cost += kReduceCycles + 2.0 * s * static_cast<double>(rows_a) * rows_b * 4.0 / kBytesPerCycle;
                 if (cost < best - 1e-9) {
                     best = cost;
                     splits = s;

@@ -10,16 +10,19 @@
 //
 // The step is bound by HBM: about 2.6 bytes move per value (bf16 in, half a
 // byte of code and 1/16 or 1/32 byte of scale out). Work unit = one "chunk" of
-// 128 rows x 4 scale blocks, which is exactly one 512-byte 128x4 scale atom:
-// a CTA of 128 threads takes a chunk, thread t owns row t of it, loads its four
-// blocks with 16-byte loads (all issued before any arithmetic), writes its
-// codes with 8- or 16-byte stores and its four scale bytes either into the
-// plain row-major matrix or into a 512-byte shared staging atom that one warp
-// writes out with 16-byte stores. The grid is persistent (the SM count times
-// the CTAs that fit on one SM) and walks chunks along K inside each 128-row band.
+// 128 rows x 4 scale blocks, which is exactly one 512-byte 128x4 scale atom.
+// A CTA of 128 threads takes a chunk; lanes run along K (a 16-byte piece each,
+// whole 128-byte lines per warp-wide load), the block maximum is reduced over
+// the block's 2-8 lanes with shuffles, and each lane stores the codes of its
+// piece (2 or 4 bytes, whole 32-byte sectors per row). The first lane of each
+// block writes the scale byte into the plain row-major matrix or into a
+// 512-byte shared staging atom that one warp writes out with 16-byte stores.
+// The grid is persistent (the SM count times the CTAs that fit on one SM) and
+// walks chunks along K inside each 128-row band.
 //
 // Exactness. Every decision is the one the fp32 definition makes:
-//   - NVFP4 scale: amax / 6 with IEEE division, then the hardware conversion
+//   - NVFP4 scale: RN(amax / 6) (by the residual step below, which gives the
+//     correctly rounded quotient), then the hardware conversion
 //     cvt.rn.satfinite.e4m3x2.f32 (round to nearest even, saturate at 448);
 //   - MXFP4 scale: the exponent field of amax (subnormals through the count of
 //     leading zeros), so floor(log2 amax) is exact;
@@ -30,8 +33,11 @@
 //     functions on the IBM RISC System/6000 processor", IBM J. Res. Dev. 34,
 //     1990: a correctly rounded reciprocal and one such correction yield the
 //     correctly rounded quotient);
-//   - the code: cvt.rn.satfinite.e2m1x2.f32 on |q| (round to nearest even,
-//     saturate at 6) with the sign bit of x put back by hand.
+//   - the code: cvt.rn.satfinite.e2m1x2.f32 on q (round to nearest even,
+//     saturate at +-6, sign kept, so -0 gives code 8), with the sign bit of x
+//     copied onto q first because the residual step turns -0 into +0.
+//   - RN(1/s) for the 127 finite E4M3 values comes from a per-CTA table filled
+//     with the correctly rounded reciprocal at kernel start.
 
 #include <cuda_runtime.h>
 
@@ -46,8 +52,9 @@ constexpr int kChunkRows = 128;    // rows per chunk = rows of one scale atom
 constexpr int kChunkBlocks = 4;    // scale blocks per chunk = columns of one scale atom
 constexpr int kAtomBytes = 512;
 
-// Four E2M1 bytes from eight non-negative values (round to nearest even, saturating at 6);
-// byte j holds value 2j in its low nibble and 2j + 1 in its high nibble.
+// Four E2M1 bytes from eight values (round to nearest even, saturating at +-6,
+// the sign kept: -0 and negatives that round to zero give code 8); byte j
+// holds value 2j in its low nibble and 2j + 1 in its high nibble.
 __device__ __forceinline__ uint32_t e2m1x8(const float (&q)[8])
 {
     uint32_t r;
@@ -78,142 +85,204 @@ __device__ __forceinline__ float e4m3_value(uint32_t c)
     return __uint_as_float(((e + 120u) << 23) | (m << 20));
 }
 
-// Sign bits of eight values placed where their codes' sign bits go.
-__device__ __forceinline__ uint32_t sign_bits8(const float (&v)[8])
+// RN(a / 6) for finite a >= 0: a * RN(1/6), then one residual step (the same
+// correctly rounded quotient as the division, by the theorem cited above).
+__device__ __forceinline__ float div6(float a)
 {
-    uint32_t s = 0;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        s |= (__float_as_uint(v[2 * j]) >> 31) << (8 * j + 3);
-        s |= (__float_as_uint(v[2 * j + 1]) >> 31) << (8 * j + 7);
-    }
-    return s;
+    const float y = 0.16666667163372039794921875f;          // RN(1/6)
+    const float q0 = a * y;
+    const float r = fmaf(-q0, 6.0f, a);
+    return fmaf(r, y, q0);
 }
 
-// The block's values as fp32 (LINES 16-byte words of raw input).
-template <bool BF16, int VEC, int LINES>
-__device__ __forceinline__ void unpack(const uint4 (&raw)[LINES], float (&v)[VEC])
+// q with the sign bit of x (the residual step of the quotient loses the sign of -0).
+__device__ __forceinline__ float with_sign_of(float q, float x)
 {
+    return __uint_as_float((__float_as_uint(q) & 0x7FFFFFFFu) | (__float_as_uint(x) & 0x80000000u));
+}
+
+// Lane geometry of one chunk (128 rows x 4 scale blocks). A lane owns a
+// 16-byte piece of a row (8 bf16 or 4 fp32 values); L consecutive lanes hold
+// one scale block, P consecutive lanes one chunk row, so every warp-wide load
+// reads whole 128-byte lines (32 / P rows of the chunk, P x 16 contiguous
+// bytes each). A pass covers 128 / P rows; 8 passes are a step, whose 8 loads
+// a thread issues before it quantises any of them.
+template <bool MX, bool BF16>
+struct Geo {
+    static constexpr int VEC = MX ? 32 : 16;
+    static constexpr int ESIZE = BF16 ? 2 : 4;
+    static constexpr int EPL = 16 / ESIZE;                 // values per lane piece: 8 or 4
+    static constexpr int L = VEC / EPL;                    // lanes per scale block: 2, 4 or 8
+    static constexpr int P = kChunkBlocks * L;             // lanes per chunk row: 8, 16 or 32
+    static constexpr int RPP = kChunkRows / P;             // chunk rows per pass (128 threads)
+    static constexpr int NSTEP = P / 8;                    // steps per chunk (P passes of RPP rows)
+    static_assert(P <= 32 && kChunkRows % P == 0, "lane geometry");
+};
+
+// The piece's values as fp32.
+template <bool BF16, int EPL>
+__device__ __forceinline__ void unpack(const uint4 &raw, float (&v)[EPL])
+{
+    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
 #pragma unroll
-    for (int l = 0; l < LINES; ++l) {
-        const uint32_t w[4] = {raw[l].x, raw[l].y, raw[l].z, raw[l].w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            if constexpr (BF16) {
-                v[8 * l + 2 * i] = __uint_as_float(w[i] << 16);
-                v[8 * l + 2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
-            } else {
-                v[4 * l + i] = __uint_as_float(w[i]);
-            }
+    for (int i = 0; i < 4; ++i) {
+        if constexpr (BF16) {
+            v[2 * i] = __uint_as_float(w[i] << 16);
+            v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+        } else {
+            v[i] = __uint_as_float(w[i]);
         }
     }
 }
 
-// One block: returns its scale byte and writes VEC / 8 words of codes.
-template <bool MX, bool BF16, int VEC, int LINES>
-__device__ __forceinline__ uint32_t quant_block(const uint4 (&raw)[LINES], uint32_t (&codes)[VEC / 8])
+// Quantises one lane piece: `amax` is the block's (already reduced over its
+// lanes); s_val / s_rcp hold each E4M3 byte's value and RN(1 / value). Returns
+// the scale byte; `out` gets EPL / 2 code bytes (low byte first).
+template <bool MX, int EPL>
+__device__ __forceinline__ uint32_t quant_piece(const float (&v)[EPL], float amax, const float *s_val,
+                                                const float *s_rcp, uint32_t &out)
 {
-    float v[VEC];
-    unpack<BF16, VEC, LINES>(raw, v);
-    float amax = 0.0f;
-#pragma unroll
-    for (int i = 0; i < VEC; ++i) amax = fmaxf(amax, fabsf(v[i]));
-
     uint32_t sc;
     float s, rcp;
     if constexpr (MX) {
         const uint32_t bits = __float_as_uint(amax);
         const int ex = static_cast<int>(bits >> 23);
-        int fl = ex - 127;                                        // floor(log2 amax), normal amax
+        int fl = ex - 127;                                              // floor(log2 amax), normal amax
         if (ex == 0) fl = (31 - __clz(static_cast<int>(bits))) - 149;   // subnormal amax
-        const int e2 = amax == 0.0f ? -127 : max(fl - 2, -127);    // at most 125 for finite amax
+        const int e2 = amax == 0.0f ? -127 : max(fl - 2, -127);          // at most 125 for finite amax
         sc = static_cast<uint32_t>(e2 + 127);
-        s = 1.0f;                                                  // unused: q = x * 2^-e2 exactly
+        s = 1.0f;                                                        // unused: q = x * 2^-e2 exactly
         rcp = __uint_as_float(static_cast<uint32_t>(127 - e2) << 23);
     } else {
-        sc = e4m3_code(amax / 6.0f);
-        s = e4m3_value(sc);
-        if (s == 0.0f) {
-#pragma unroll
-            for (int w = 0; w < VEC / 8; ++w) codes[w] = 0;        // zero scale: all codes 0
+        sc = e4m3_code(div6(amax));
+        s = s_val[sc];
+        if (s == 0.0f) {                                                 // zero scale: all codes 0
+            out = 0;
             return sc;
         }
-        rcp = __frcp_rn(s);
+        rcp = s_rcp[sc];
     }
+    float q[8];
 #pragma unroll
-    for (int w = 0; w < VEC / 8; ++w) {
-        float q[8], x8[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const float a = fabsf(v[8 * w + i]);
-            x8[i] = v[8 * w + i];
+    for (int i = 0; i < 8; ++i) {
+        if (i < EPL) {
+            const float x = v[i];
             if constexpr (MX) {
-                q[i] = a * rcp;
+                q[i] = x * rcp;
             } else {
-                const float q0 = a * rcp;
-                const float r = fmaf(-q0, s, a);
-                q[i] = fmaf(r, rcp, q0);
+                const float q0 = x * rcp;
+                const float r = fmaf(-q0, s, x);
+                q[i] = with_sign_of(fmaf(r, rcp, q0), x);
             }
+        } else {
+            q[i] = 0.0f;
         }
-        codes[w] = e2m1x8(q) | sign_bits8(x8);
     }
+    out = e2m1x8(q);
     return sc;
 }
 
+// Per-thread work of one step: the 8 pieces (8 x 16 bytes) of passes
+// 8 * st .. 8 * st + 7 of chunk c.
+template <bool MX, bool BF16>
+struct Work {
+    using G = Geo<MX, BF16>;
+    const uint8_t *__restrict__ X;
+    uint8_t *__restrict__ codes;
+    uint8_t *__restrict__ sf;
+    int64_t rows, K, nb, kc4;
+    int atom_layout;
+
+    __device__ __forceinline__ void load(int64_t c, int st, uint4 (&raw)[8]) const
+    {
+        const int t = threadIdx.x, piece = t % G::P;
+        const int64_t rb = c / kc4, b0 = (c - rb * kc4) * kChunkBlocks;
+        const bool col_ok = b0 + piece / G::L < nb;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            const int64_t r = rb * kChunkRows + (st * 8 + q) * G::RPP + t / G::P;
+            raw[q] = make_uint4(0, 0, 0, 0);
+            if (r < rows && col_ok)
+                raw[q] = __ldg(reinterpret_cast<const uint4 *>(X + (r * K + b0 * G::VEC) * G::ESIZE) + piece);
+        }
+    }
+
+    __device__ __forceinline__ void quantise(int64_t c, int st, const uint4 (&raw)[8], uint8_t *staging,
+                                             const float *s_val, const float *s_rcp) const
+    {
+        const int t = threadIdx.x, piece = t % G::P, j = piece / G::L;
+        const bool leader = piece % G::L == 0;                  // writes the block's scale byte
+        const int64_t rb = c / kc4, b0 = (c - rb * kc4) * kChunkBlocks;
+        const bool col_ok = b0 + j < nb;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            const int rr = (st * 8 + q) * G::RPP + t / G::P;     // row within the chunk
+            const int64_t r = rb * kChunkRows + rr;
+            const bool ok = r < rows && col_ok;
+            float v[G::EPL];
+            unpack<BF16, G::EPL>(raw[q], v);
+            float amax = 0.0f;
+#pragma unroll
+            for (int i = 0; i < G::EPL; ++i) amax = fmaxf(amax, fabsf(v[i]));
+#pragma unroll
+            for (int o = 1; o < G::L; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+            uint32_t out;
+            const uint32_t sc = quant_piece<MX, G::EPL>(v, amax, s_val, s_rcp, out);
+            if (ok) {
+                uint8_t *dst = codes + r * (K / 2) + (b0 * G::VEC) / 2 + piece * (G::EPL / 2);
+                if constexpr (BF16)
+                    *reinterpret_cast<uint32_t *>(dst) = out;
+                else
+                    *reinterpret_cast<uint16_t *>(dst) = static_cast<uint16_t>(out);
+            }
+            if (leader) {
+                if (atom_layout)
+                    staging[(rr & 31) * 16 + (rr >> 5) * 4 + j] = ok ? static_cast<uint8_t>(sc) : 0;
+                else if (ok)
+                    sf[r * nb + b0 + j] = static_cast<uint8_t>(sc);
+            }
+        }
+    }
+
+    // After a chunk's last step: the staged atom goes out in 16-byte stores.
+    __device__ __forceinline__ void finish(int64_t c, const uint8_t *staging) const
+    {
+        if (!atom_layout) return;
+        __syncthreads();
+        if (threadIdx.x < 32)
+            reinterpret_cast<uint4 *>(sf + c * kAtomBytes)[threadIdx.x] = reinterpret_cast<const uint4 *>(staging)[threadIdx.x];
+        __syncthreads();
+    }
+};
+
+// Persistent loop over chunks; each step's 8 loads are issued together before
+// the step is quantised (more resident CTAs, not a second register buffer,
+// keep the loads of other CTAs in flight meanwhile).
 template <bool MX, bool BF16>
 __global__ void __launch_bounds__(kChunkRows) quantize_kernel(const uint8_t *__restrict__ X,
                                                               uint8_t *__restrict__ codes,
                                                               uint8_t *__restrict__ sf, int64_t rows,
                                                               int64_t K, int64_t nb, int64_t kc4,
-                                                              int64_t chunks, int atom_layout, int plain_words)
+                                                              int64_t chunks, int atom_layout)
 {
-    constexpr int VEC = MX ? 32 : 16;
-    constexpr int ESIZE = BF16 ? 2 : 4;
-    constexpr int LINES = VEC * ESIZE / 16;            // 16-byte input words per block
-    __shared__ uint32_t staging[kChunkRows];            // one scale atom
-    const int t = threadIdx.x;
+    using G = Geo<MX, BF16>;
+    __shared__ __align__(16) uint8_t staging[kAtomBytes];    // one scale atom
+    __shared__ float s_val[128], s_rcp[128];                  // E4M3 byte -> value, RN(1 / value)
+    if (!MX) {
+        const float val = e4m3_value(threadIdx.x);
+        s_val[threadIdx.x] = val;
+        s_rcp[threadIdx.x] = val != 0.0f ? __frcp_rn(val) : 0.0f;
+        __syncthreads();
+    }
+    const Work<MX, BF16> w{X, codes, sf, rows, K, nb, kc4, atom_layout};
     for (int64_t c = blockIdx.x; c < chunks; c += gridDim.x) {
-        const int64_t rb = c / kc4, cb = c - rb * kc4;
-        const int64_t r = rb * kChunkRows + t;
-        const int64_t b0 = cb * kChunkBlocks;
-        const int nblk = nb - b0 < kChunkBlocks ? static_cast<int>(nb - b0) : kChunkBlocks;
-        uint32_t scales = 0;
-        if (r < rows) {
-            const uint4 *src = reinterpret_cast<const uint4 *>(X + (r * K + b0 * VEC) * ESIZE);
-            uint4 raw[kChunkBlocks][LINES];
-#pragma unroll
-            for (int j = 0; j < kChunkBlocks; ++j)
-                if (j < nblk)
-#pragma unroll
-                    for (int l = 0; l < LINES; ++l) raw[j][l] = __ldg(src + j * LINES + l);
-            uint8_t *dst = codes + r * (K / 2) + b0 * (VEC / 2);
-#pragma unroll
-            for (int j = 0; j < kChunkBlocks; ++j) {
-                if (j < nblk) {
-                    uint32_t w[VEC / 8];
-                    scales |= quant_block<MX, BF16, VEC, LINES>(raw[j], w) << (8 * j);
-                    if constexpr (MX)
-                        *reinterpret_cast<uint4 *>(dst + j * 16) = make_uint4(w[0], w[1], w[2], w[3]);
-                    else
-                        *reinterpret_cast<uint2 *>(dst + j * 8) = make_uint2(w[0], w[1]);
-                }
-            }
+#pragma unroll 1
+        for (int st = 0; st < G::NSTEP; ++st) {
+            uint4 raw[8];
+            w.load(c, st, raw);
+            w.quantise(c, st, raw, staging, s_val, s_rcp);
         }
-        if (atom_layout) {
-            // row t of the atom: line t % 32, byte group t / 32 (columns in byte order)
-            staging[(t & 31) * 4 + (t >> 5)] = scales;
-            __syncthreads();
-            if (t < 32)
-                reinterpret_cast<uint4 *>(sf + c * kAtomBytes)[t] = reinterpret_cast<const uint4 *>(staging)[t];
-            __syncthreads();
-        } else if (r < rows) {
-            uint8_t *row = sf + r * nb + b0;
-            if (plain_words && nblk == kChunkBlocks) {
-                *reinterpret_cast<uint32_t *>(row) = scales;
-            } else {
-                for (int j = 0; j < nblk; ++j) row[j] = static_cast<uint8_t>(scales >> (8 * j));
-            }
-        }
+        w.finish(c, staging);
     }
 }
 
@@ -243,8 +312,7 @@ extern "C" fp4_status fp4_quantize(fp4_format fmt, const void *X, fp4_in_dtype i
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
         return FP4_ERR_NO_DEVICE;
-    using Kernel = void (*)(const uint8_t *, uint8_t *, uint8_t *, int64_t, int64_t, int64_t, int64_t, int64_t,
-                            int, int);
+    using Kernel = void (*)(const uint8_t *, uint8_t *, uint8_t *, int64_t, int64_t, int64_t, int64_t, int64_t, int);
     const Kernel kern = mx ? (in == FP4_IN_BF16 ? quantize_kernel<true, true> : quantize_kernel<true, false>)
                            : (in == FP4_IN_BF16 ? quantize_kernel<false, true> : quantize_kernel<false, false>);
     // persistent grid: every SM filled to the kernel's occupancy
@@ -255,8 +323,7 @@ extern "C" fp4_status fp4_quantize(fp4_format fmt, const void *X, fp4_in_dtype i
     }
     const unsigned blocks = static_cast<unsigned>(std::min<int64_t>(chunks, int64_t(sms) * per_sm));
     const int atom = layout == FP4_SF_ATOM;
-    const int words = (nb % 4 == 0) && ((reinterpret_cast<uintptr_t>(sf) & 3u) == 0);
     kern<<<blocks, kChunkRows, 0, stream>>>(static_cast<const uint8_t *>(X), static_cast<uint8_t *>(codes),
-                                            static_cast<uint8_t *>(sf), rows, K, nb, kc4, chunks, atom, words);
+                                            static_cast<uint8_t *>(sf), rows, K, nb, kc4, chunks, atom);
     return cudaGetLastError() == cudaSuccess ? FP4_OK : FP4_ERR_CUDA;
 }
