@@ -258,7 +258,7 @@ __device__ __forceinline__ void tmem_load_cols(uint32_t taddr, uint32_t *v)
 // element count of 16 bytes.
 __device__ __forceinline__ void store_chunk32(uint8_t *stg, const uint32_t (&w)[8], void *out, int64_t ldo,
                                               int esize, int row0, int col0, int half_cols, int rows, int cols,
-                                              int lane)
+                                              int lane, uint64_t policy)
 {
     const int sw = (lane >> 2) & 1;
     *reinterpret_cast<uint4 *>(stg + lane * 32 + (sw << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
@@ -271,7 +271,7 @@ __device__ __forceinline__ void store_chunk32(uint8_t *stg, const uint32_t (&w)[
         const int row = row0 + r, col = col0 + half * half_cols;
         const uint4 val = *reinterpret_cast<const uint4 *>(stg + r * 32 + ((half ^ ((r >> 2) & 1)) << 4));
         if (row < rows && col < cols)
-            *reinterpret_cast<uint4 *>(static_cast<char *>(out) + (static_cast<int64_t>(row) * ldo + col) * esize) = val;
+            st_global_v4_hint(static_cast<char *>(out) + (static_cast<int64_t>(row) * ldo + col) * esize, val, policy);
     }
     __syncwarp();
 }
@@ -406,6 +406,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t desc_sfb0 = smem_desc(base + C::OFF_SFB, 0, 128, 0);
             int stage = 0;
             int acc = 0;
+            uint32_t acc_phase = 0;
             uint32_t consumed = 0, ready = 0;    // stages issued / stages known to have landed
             bool ok = true;
             for (int u = pair; ok && u < args.units; u += npairs) {
@@ -413,10 +414,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 unit_coords(args, u, ta, tb, split);
                 const int kt0 = split * args.kps;
                 const int kt1 = min(kt0 + args.kps, args.k_tiles);
+                // the epilogue has drained this accumulator (once per tile)
+                if (!wait_cluster(bar_acc_empty + 8 * acc, acc_phase ^ 1u, args.wait_ns, abort_flag)) break;
                 const uint32_t d_tmem = tmem + static_cast<uint32_t>(acc * BN);
                 for (int kt = kt0; kt < kt1; kt += KT) {
-                    // The waiter warp has seen this stage land (and, for a unit's first
-                    // stage, the accumulator drained) once its count passes `consumed`.
+                    // The waiter warp has seen this stage land once its count passes `consumed`.
                     if (ready == consumed) {
                         ready = take_credit(ready_addr, consumed, args.wait_ns, abort_flag);
                         if (ready == 0) {
@@ -457,7 +459,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (!ok) break;
                 tc_commit<CG>(bar_acc_full + 8 * acc);
-                if (C::ACC_BUFS == 2) acc ^= 1;
+                if (C::ACC_BUFS == 2) {
+                    acc ^= 1;
+                    if (acc == 0) acc_phase ^= 1u;
+                } else {
+                    acc_phase ^= 1u;
+                }
             }
             // Every MMA and scale copy this thread issued completes before teardown.
             tc_commit<CG>(bar_drain, 1);
@@ -465,16 +472,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == kWaiterWarp) {
         // ------------------------------------------------------------ waiter
-        // Waits, in the MMA issue order, for each unit's accumulator to be
-        // drained and for each stage to land, and publishes the running count.
-        // The MMA thread then never blocks in an mbarrier wait: on this part a
-        // wait in the issuing thread costs about 200 cycles in which the tensor
-        // core runs dry.
+        // Waits, in the MMA issue order, for each stage to land and publishes
+        // the running count, so that the MMA thread blocks in an mbarrier wait
+        // only once per tile (for the accumulator): on this part a wait in the
+        // issuing thread costs about 200 cycles in which the tensor core runs dry.
         if (lane == 0 && rank == 0) {
             int stage = 0;
             uint32_t phase = 0;
-            int acc = 0;
-            uint32_t acc_phase = 0;
             uint32_t seen = 0;
             bool ok = true;
             for (int u = pair; ok && u < args.units; u += npairs) {
@@ -482,7 +486,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 unit_coords(args, u, ta, tb, split);
                 const int kt0 = split * args.kps;
                 const int kt1 = min(kt0 + args.kps, args.k_tiles);
-                if (!wait_cluster(bar_acc_empty + 8 * acc, acc_phase ^ 1u, args.wait_ns, abort_flag)) break;
                 for (int kt = kt0; kt < kt1; kt += KT) {
                     if (!wait(bar_full + 8 * stage, phase, args.wait_ns, abort_flag)) {
                         ok = false;
@@ -494,12 +497,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                         phase ^= 1u;
                     }
                 }
-                if (C::ACC_BUFS == 2) {
-                    acc ^= 1;
-                    if (acc == 0) acc_phase ^= 1u;
-                } else {
-                    acc_phase ^= 1u;
-                }
             }
         }
     } else {
@@ -508,6 +505,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int h = (warp - 2) >> 2;                   // which half of the tile's columns
         const uint32_t acc_empty0 = CG == 2 ? mapa_shared(bar_acc_empty, 0) : bar_acc_empty;
         uint8_t *const stg_ptr = base_ptr + C::OFF_STG + (warp - 2) * kStgBytes;
+        // D is written once and not read again here: evict it from L2 first, so the
+        // operand tiles that other CTAs still load stay resident.
+        const uint64_t d_policy = policy_evict_first();
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int u = pair; u < args.units; u += npairs) {
@@ -547,7 +547,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 w[i] = *reinterpret_cast<uint32_t *>(&p);
                             }
                             store_chunk32(stg_ptr, w, args.out, args.ldo, 2, row_base, col0 + 16 * ch, 8, args.rows_a,
-                                          args.rows_b, lane);
+                                          args.rows_b, lane, d_policy);
                         }
                     } else {
 #pragma unroll
@@ -556,7 +556,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                             for (int i = 0; i < 8; ++i) w[i] = __float_as_uint(__uint_as_float(v[8 * ch + i]) * args.alpha);
                             store_chunk32(stg_ptr, w, args.out, args.ldo, 4, row_base, col0 + 8 * ch, 4, args.rows_a,
-                                          args.rows_b, lane);
+                                          args.rows_b, lane, d_policy);
                         }
                     }
                 } else if (args.mode == kEpiSplitK) {
@@ -565,20 +565,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                     float *ws = static_cast<float *>(args.out) + split * args.split_stride + ra;
 #pragma unroll
                     for (int i = 0; i < C::COLS_WARP; ++i)
-                        if (col0 + i < args.rows_b) ws[static_cast<int64_t>(col0 + i) * args.ldo] = __uint_as_float(v[i]);
+                        if (col0 + i < args.rows_b)
+                            st_global_b32_hint(ws + static_cast<int64_t>(col0 + i) * args.ldo, v[i], d_policy);
                 } else if (args.bf16) {
                     __nv_bfloat16 *d = static_cast<__nv_bfloat16 *>(args.out) + ra;
 #pragma unroll
                     for (int i = 0; i < C::COLS_WARP; ++i)
                         if (col0 + i < args.rows_b)
-                            d[static_cast<int64_t>(col0 + i) * args.ldo] =
-                                __float2bfloat16_rn(__uint_as_float(v[i]) * args.alpha);
+                            st_global_b16_hint(d + static_cast<int64_t>(col0 + i) * args.ldo,
+                                               __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v[i]) * args.alpha)),
+                                               d_policy);
                 } else {
                     float *d = static_cast<float *>(args.out) + ra;
 #pragma unroll
                     for (int i = 0; i < C::COLS_WARP; ++i)
                         if (col0 + i < args.rows_b)
-                            d[static_cast<int64_t>(col0 + i) * args.ldo] = __uint_as_float(v[i]) * args.alpha;
+                            st_global_b32_hint(d + static_cast<int64_t>(col0 + i) * args.ldo,
+                                               __float_as_uint(__uint_as_float(v[i]) * args.alpha), d_policy);
                 }
             }
             if (C::ACC_BUFS == 2) {

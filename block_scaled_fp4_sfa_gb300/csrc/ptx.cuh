@@ -193,6 +193,24 @@ __device__ __forceinline__ uint64_t policy_evict_first()
     return p;
 }
 
+// Global stores with an L2 eviction-priority hint (a createpolicy value).
+__device__ __forceinline__ void st_global_v4_hint(void *p, const uint4 &v, uint64_t policy)
+{
+    asm volatile("st.global.L2::cache_hint.v4.u32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(p), "r"(v.x), "r"(v.y),
+                 "r"(v.z), "r"(v.w), "l"(policy)
+                 : "memory");
+}
+
+__device__ __forceinline__ void st_global_b32_hint(void *p, uint32_t v, uint64_t policy)
+{
+    asm volatile("st.global.L2::cache_hint.b32 [%0], %1, %2;" ::"l"(p), "r"(v), "l"(policy) : "memory");
+}
+
+__device__ __forceinline__ void st_global_b16_hint(void *p, uint16_t v, uint64_t policy)
+{
+    asm volatile("st.global.L2::cache_hint.b16 [%0], %1, %2;" ::"l"(p), "h"(v), "l"(policy) : "memory");
+}
+
 // Contiguous global -> shared bulk copy (16-byte aligned addresses, size % 16 == 0).
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar)
 {
