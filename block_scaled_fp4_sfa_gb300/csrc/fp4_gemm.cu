@@ -46,6 +46,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
@@ -89,6 +90,16 @@ struct Args {
     int32_t bf16;            // output type for modes 0 and 1
     int32_t mode;            // EpiMode
     float alpha;
+    // Split tail (direct mode): units 0 .. split_units-1 are the two K halves of
+    // the first split_units / 2 tiles (the tiles beyond the last full wave, run
+    // first so that their extra epilogue work overlaps later tiles). The first
+    // half leaves its fp32 partial in tail_ws and publishes `epoch` in its flag;
+    // the second half adds it.
+    int32_t split_units;
+    int32_t kh;                          // k-tiles of a first half
+    float *tail_ws;                      // [tail tile][CTA of the pair][BN][128]
+    unsigned long long *tail_flags;      // [tail tile][CTA of the pair]
+    unsigned long long epoch;            // this launch's flag value
 };
 
 template <int CG, int BN, bool MX, int KT>
@@ -214,6 +225,25 @@ __device__ __noinline__ uint32_t take_credit(uint32_t ready_addr, uint32_t consu
     }
 }
 
+// Bounded wait until *flag == epoch (acquire, GPU scope): the first half of a
+// split tail tile has left its partial.
+__device__ __noinline__ bool wait_flag(const unsigned long long *flag, unsigned long long epoch, uint64_t limit_ns,
+                                       volatile uint32_t *abort_flag)
+{
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (ld_acquire_gpu_u64(flag) == epoch) return true;
+        if ((it & 63u) == 0) {
+            if (*abort_flag != 0) return false;
+            if (global_timer_ns() - t0 > limit_ns) {
+                record_error(FP4_ERR_TIMEOUT);
+                *abort_flag = 1;
+                return false;
+            }
+        }
+    }
+}
+
 // Unit u -> (slot-A tile, slot-B tile, split). Splits are outermost; inside a
 // split, tiles go in groups of `group_b` slot-B tiles with slot-A tiles
 // running across each group, so the CTAs in flight share operand rows in L2.
@@ -229,6 +259,27 @@ __device__ __forceinline__ void unit_coords(const Args &a, int u, int &ta, int &
     const int gw = min(a.group_b, a.tiles_b - b0);
     tb = b0 + r % gw;
     ta = r / gw;
+}
+
+// Unit u -> its tile and k-tile range. half = -1 for a whole tile (or a
+// split-K unit); 0 / 1 for the first / second K half of a split tile, whose
+// index among the split tiles is tidx.
+__device__ __forceinline__ void unit_work(const Args &a, int u, int &ta, int &tb, int &split, int &kt0, int &kt1,
+                                          int &half, int &tidx)
+{
+    if (u >= a.split_units) {
+        unit_coords(a, u - a.split_units / 2, ta, tb, split);
+        kt0 = split * a.kps;
+        kt1 = min(kt0 + a.kps, a.k_tiles);
+        half = -1;
+        tidx = 0;
+        return;
+    }
+    tidx = u >> 1;
+    half = u & 1;
+    unit_coords(a, tidx, ta, tb, split);
+    kt0 = half ? a.kh : 0;
+    kt1 = half ? a.k_tiles : a.kh;
 }
 
 // Loads N consecutive 32-bit TMEM columns of this warp's 32 lanes.
@@ -345,10 +396,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t filled = 0, fill_parity = 0;
             bool ok = true;
             for (int u = pair; ok && u < args.units; u += npairs) {
-                int ta, tb, split;
-                unit_coords(args, u, ta, tb, split);
-                const int kt0 = split * args.kps;
-                const int kt1 = min(kt0 + args.kps, args.k_tiles);
+                int ta, tb, split, kt0, kt1, half, tidx;
+                unit_work(args, u, ta, tb, split, kt0, kt1, half, tidx);
                 const int rba = ta * CG + static_cast<int>(rank);       // this CTA's 128-row block of slot A
                 const int row_a = rba * kBM;
                 const int row_b = tb * BN + static_cast<int>(rank) * C::BN_CTA;
@@ -410,10 +459,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t consumed = 0, ready = 0;    // stages issued / stages known to have landed
             bool ok = true;
             for (int u = pair; ok && u < args.units; u += npairs) {
-                int ta, tb, split;
-                unit_coords(args, u, ta, tb, split);
-                const int kt0 = split * args.kps;
-                const int kt1 = min(kt0 + args.kps, args.k_tiles);
+                int ta, tb, split, kt0, kt1, half, tidx;
+                unit_work(args, u, ta, tb, split, kt0, kt1, half, tidx);
                 // the epilogue has drained this accumulator (once per tile)
                 if (!wait_cluster(bar_acc_empty + 8 * acc, acc_phase ^ 1u, args.wait_ns, abort_flag)) break;
                 const uint32_t d_tmem = tmem + static_cast<uint32_t>(acc * BN);
@@ -482,10 +529,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t seen = 0;
             bool ok = true;
             for (int u = pair; ok && u < args.units; u += npairs) {
-                int ta, tb, split;
-                unit_coords(args, u, ta, tb, split);
-                const int kt0 = split * args.kps;
-                const int kt1 = min(kt0 + args.kps, args.k_tiles);
+                int ta, tb, split, kt0, kt1, half, tidx;
+                unit_work(args, u, ta, tb, split, kt0, kt1, half, tidx);
                 for (int kt = kt0; kt < kt1; kt += KT) {
                     if (!wait(bar_full + 8 * stage, phase, args.wait_ns, abort_flag)) {
                         ok = false;
@@ -511,8 +556,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int u = pair; u < args.units; u += npairs) {
-            int ta, tb, split;
-            unit_coords(args, u, ta, tb, split);
+            int ta, tb, split, kt0, kt1, half, tidx;
+            unit_work(args, u, ta, tb, split, kt0, kt1, half, tidx);
             if (!wait(bar_acc_full + 8 * acc, acc_phase, args.wait_ns, abort_flag)) break;
             tc_fence_after();
             // Drain this warp's 32 lanes x BN/2 columns, then release the accumulator.
@@ -529,59 +574,89 @@ __global__ void __launch_bounds__(kThreads, 1)
                 else
                     mbar_arrive(bar_acc_empty + 8 * acc);
             }
-            const int row_base = (ta * CG + static_cast<int>(rank)) * kBM + 32 * q;   // this warp's first row
-            const int ra = row_base + lane;                                            // slot-A row of this lane
-            const int col0 = tb * BN + h * C::COLS_WARP;                                // first slot-B row
-            if (args.mode == kEpiRows || ra < args.rows_a) {       // the row stores are warp-collective
-                if (args.mode == kEpiRows) {
-                    // D rows of this warp in 32-byte column chunks through the staging
-                    if (args.bf16) {
+            // Split tail: a first half parks its fp32 partial (this warp's 32 rows x
+            // BN/2 columns, column-major so a fixed column is 32 consecutive floats)
+            // and raises its flag; the second half's matching warp adds it.
+            bool store_d = true;
+            if (CG == 1 && half >= 0) {   // (pairs never split: their epilogue has no registers to spare)
+                const int slot = tidx * CG + static_cast<int>(rank);
+                float *part = args.tail_ws + (static_cast<int64_t>(slot) * BN + h * C::COLS_WARP) * kBM + 32 * q + lane;
+                unsigned long long *flag = args.tail_flags + slot * kEpiWarps + (warp - 2);
+                if (half == 0) {
 #pragma unroll
-                        for (int ch = 0; ch < C::COLS_WARP / 16; ++ch) {
-                            uint32_t w[8];
-#pragma unroll
-                            for (int i = 0; i < 8; ++i) {
-                                __nv_bfloat162 p = __floats2bfloat162_rn(
-                                    __uint_as_float(v[16 * ch + 2 * i]) * args.alpha,
-                                    __uint_as_float(v[16 * ch + 2 * i + 1]) * args.alpha);
-                                w[i] = *reinterpret_cast<uint32_t *>(&p);
-                            }
-                            store_chunk32(stg_ptr, w, args.out, args.ldo, 2, row_base, col0 + 16 * ch, 8, args.rows_a,
-                                          args.rows_b, lane, d_policy);
-                        }
-                    } else {
-#pragma unroll
-                        for (int ch = 0; ch < C::COLS_WARP / 8; ++ch) {
-                            uint32_t w[8];
-#pragma unroll
-                            for (int i = 0; i < 8; ++i) w[i] = __float_as_uint(__uint_as_float(v[8 * ch + i]) * args.alpha);
-                            store_chunk32(stg_ptr, w, args.out, args.ldo, 4, row_base, col0 + 8 * ch, 4, args.rows_a,
-                                          args.rows_b, lane, d_policy);
-                        }
-                    }
-                } else if (args.mode == kEpiSplitK) {
-                    // fp32 partials, transposed: for a fixed column the 32 lanes of a
-                    // warp write 32 consecutive elements
-                    float *ws = static_cast<float *>(args.out) + split * args.split_stride + ra;
-#pragma unroll
-                    for (int i = 0; i < C::COLS_WARP; ++i)
-                        if (col0 + i < args.rows_b)
-                            st_global_b32_hint(ws + static_cast<int64_t>(col0 + i) * args.ldo, v[i], d_policy);
-                } else if (args.bf16) {
-                    __nv_bfloat16 *d = static_cast<__nv_bfloat16 *>(args.out) + ra;
-#pragma unroll
-                    for (int i = 0; i < C::COLS_WARP; ++i)
-                        if (col0 + i < args.rows_b)
-                            st_global_b16_hint(d + static_cast<int64_t>(col0 + i) * args.ldo,
-                                               __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v[i]) * args.alpha)),
-                                               d_policy);
+                    for (int i = 0; i < C::COLS_WARP; ++i) __stcg(part + i * kBM, __uint_as_float(v[i]));
+                    __threadfence();
+                    __syncwarp();
+                    if (lane == 0) st_release_gpu_u64(flag, args.epoch);
+                    store_d = false;
                 } else {
-                    float *d = static_cast<float *>(args.out) + ra;
+                    bool ok = true;
+                    if (lane == 0) ok = wait_flag(flag, args.epoch, args.wait_ns, abort_flag);
+                    ok = __shfl_sync(0xFFFFFFFFu, ok, 0) && ld_acquire_gpu_u64(flag) == args.epoch;
+                    if (ok) {
 #pragma unroll
-                    for (int i = 0; i < C::COLS_WARP; ++i)
-                        if (col0 + i < args.rows_b)
-                            st_global_b32_hint(d + static_cast<int64_t>(col0 + i) * args.ldo,
-                                               __float_as_uint(__uint_as_float(v[i]) * args.alpha), d_policy);
+                        for (int i = 0; i < C::COLS_WARP; ++i)
+                            v[i] = __float_as_uint(__uint_as_float(v[i]) + __ldcg(part + i * kBM));
+                    }
+                }
+            }
+            if (store_d) {
+                const int row_base = (ta * CG + static_cast<int>(rank)) * kBM + 32 * q;   // this warp's first row
+                const int ra = row_base + lane;                                            // slot-A row of this lane
+                const int col0 = tb * BN + h * C::COLS_WARP;                                // first slot-B row
+                if (args.mode == kEpiRows || ra < args.rows_a) {       // the row stores are warp-collective
+                    if (args.mode == kEpiRows) {
+                        // D rows of this warp in 32-byte column chunks through the staging
+                        if (args.bf16) {
+#pragma unroll
+                            for (int ch = 0; ch < C::COLS_WARP / 16; ++ch) {
+                                uint32_t w[8];
+#pragma unroll
+                                for (int i = 0; i < 8; ++i) {
+                                    __nv_bfloat162 p = __floats2bfloat162_rn(
+                                        __uint_as_float(v[16 * ch + 2 * i]) * args.alpha,
+                                        __uint_as_float(v[16 * ch + 2 * i + 1]) * args.alpha);
+                                    w[i] = *reinterpret_cast<uint32_t *>(&p);
+                                }
+                                store_chunk32(stg_ptr, w, args.out, args.ldo, 2, row_base, col0 + 16 * ch, 8,
+                                              args.rows_a, args.rows_b, lane, d_policy);
+                            }
+                        } else {
+#pragma unroll
+                            for (int ch = 0; ch < C::COLS_WARP / 8; ++ch) {
+                                uint32_t w[8];
+#pragma unroll
+                                for (int i = 0; i < 8; ++i)
+                                    w[i] = __float_as_uint(__uint_as_float(v[8 * ch + i]) * args.alpha);
+                                store_chunk32(stg_ptr, w, args.out, args.ldo, 4, row_base, col0 + 8 * ch, 4,
+                                              args.rows_a, args.rows_b, lane, d_policy);
+                            }
+                        }
+                    } else if (args.mode == kEpiSplitK) {
+                        // fp32 partials, transposed: for a fixed column the 32 lanes of a
+                        // warp write 32 consecutive elements
+                        float *ws = static_cast<float *>(args.out) + split * args.split_stride + ra;
+#pragma unroll
+                        for (int i = 0; i < C::COLS_WARP; ++i)
+                            if (col0 + i < args.rows_b)
+                                st_global_b32_hint(ws + static_cast<int64_t>(col0 + i) * args.ldo, v[i], d_policy);
+                    } else if (args.bf16) {
+                        __nv_bfloat16 *d = static_cast<__nv_bfloat16 *>(args.out) + ra;
+#pragma unroll
+                        for (int i = 0; i < C::COLS_WARP; ++i)
+                            if (col0 + i < args.rows_b)
+                                st_global_b16_hint(
+                                    d + static_cast<int64_t>(col0 + i) * args.ldo,
+                                    __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v[i]) * args.alpha)),
+                                    d_policy);
+                    } else {
+                        float *d = static_cast<float *>(args.out) + ra;
+#pragma unroll
+                        for (int i = 0; i < C::COLS_WARP; ++i)
+                            if (col0 + i < args.rows_b)
+                                st_global_b32_hint(d + static_cast<int64_t>(col0 + i) * args.ldo,
+                                                   __float_as_uint(__uint_as_float(v[i]) * args.alpha), d_policy);
+                    }
                 }
             }
             if (C::ACC_BUFS == 2) {
@@ -662,6 +737,7 @@ namespace {
 
 std::mutex g_mu;
 int64_t g_wait_ms = -1;
+std::atomic<unsigned long long> g_epoch{0};   // per-launch value of the split-tail flags
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
 constexpr int kNumKernels = 20;   // kernel variants that can be launched (see kernel_index)
@@ -782,8 +858,10 @@ struct Maps {
 };
 
 template <int CG, int BN, bool MX, int KT>
+// With `slots_out` set, only reports how many CTA groups a launch can keep
+// resident (after the cap) and launches nothing.
 cudaError_t launch_gemm(DeviceInfo &info, int kidx, int units, int cap, const Maps &m, const Args &args,
-                        cudaStream_t stream)
+                        cudaStream_t stream, int *slots_out)
 {
     using C = Cfg<CG, BN, MX, KT>;
     auto kern = fp4_gemm_kernel<CG, BN, MX, KT>;
@@ -814,6 +892,10 @@ cudaError_t launch_gemm(DeviceInfo &info, int kidx, int units, int cap, const Ma
         info.attr_set[kidx] = true;
     }
     const int slots = info.max_clusters[kidx];
+    if (slots_out) {
+        *slots_out = cap > 0 ? std::max(1, std::min(slots, cap / CG)) : slots;
+        return cudaSuccess;
+    }
     int groups = std::min(units, slots);
     if (cap > 0) groups = std::min(groups, std::max(1, cap / CG));
     groups = std::max(groups, 1);
@@ -840,10 +922,11 @@ int kernel_index(int cg, int bn, bool mx, int kt)
 }
 
 cudaError_t launch_by_cfg(int cg, int bn, bool mx, int kt, DeviceInfo &info, int units, int cap, const Maps &m,
-                          const Args &args, cudaStream_t stream)
+                          const Args &args, cudaStream_t stream, int *slots_out = nullptr)
 {
     const int k = kernel_index(cg, bn, mx, kt);
-#define FP4_LAUNCH(CG_, BN_, MX_, KT_) return launch_gemm<CG_, BN_, MX_, KT_>(info, k, units, cap, m, args, stream)
+#define FP4_LAUNCH(CG_, BN_, MX_, KT_) \
+    return launch_gemm<CG_, BN_, MX_, KT_>(info, k, units, cap, m, args, stream, slots_out)
     if (cg == 2) {
         if (kt == 2) {
             if (bn == 256) FP4_LAUNCH(2, 256, true, 2);
@@ -915,7 +998,10 @@ fp4_status make_plan(int64_t M, int64_t N, int64_t K, bool rows_ok, bool mx, int
     if (bn_index(bn) < 0) return FP4_ERR_INVALID_ARG;
     if (rows_b > bn && bn < 128) return FP4_ERR_UNSUPPORTED;       // N-side tiles must start on scale blocks
     p.bn = bn;
-    const int cg = (cfg && cfg->cta_group) ? cfg->cta_group : ((bn >= 128 && rows_a > 128) ? 2 : 1);
+    // CTA pairs for MXFP4 (with two k-tiles per TMA load); NVFP4's issue rate per SM is
+    // the same with one CTA per MMA, which also takes the split tail.
+    const int cg = (cfg && cfg->cta_group) ? cfg->cta_group
+                                           : ((bn >= 128 && rows_a > 128 && (mx || p.swap)) ? 2 : 1);
     if (cg != 1 && cg != 2) return FP4_ERR_INVALID_ARG;
     if (cg == 2 && bn < 128) return FP4_ERR_UNSUPPORTED;
     p.cg = cg;
@@ -1015,7 +1101,31 @@ fp4_status gemm_impl(fp4_format fmt, int prepacked, const void *A, const void *s
     const size_t atoms_a = static_cast<size_t>(rb_a * kc4 * kAtomBytes);
     const size_t atoms_b = static_cast<size_t>(rb_b * kc4 * kAtomBytes);
     const size_t ws_bytes = plan.splits > 1 ? static_cast<size_t>(plan.splits) * rows_a * rows_b * 4 : 0;
-    const size_t scratch_bytes = (prepacked ? 0 : atoms_a + atoms_b) + ws_bytes;
+    size_t scratch_bytes = (prepacked ? 0 : atoms_a + atoms_b) + ws_bytes;
+
+    // Split tail (direct mode): when the last wave of tiles fills at most half of
+    // the resident CTA groups, each of its tiles runs as two K halves on two
+    // groups, so the wave ends after about half a tile.
+    const int64_t tiles = cdiv(rows_a, kBM * plan.cg) * cdiv(rows_b, plan.bn);
+    const int64_t k_tiles = cdiv(K, kBK);
+    int64_t tail = 0;
+    if (!plan.swap && plan.splits == 1 && plan.cg == 1 && k_tiles >= 2) {
+        int slots = 0;
+        Maps none;
+        Args none_args;
+        std::memset(&none, 0, sizeof none);
+        std::memset(&none_args, 0, sizeof none_args);
+        if (launch_by_cfg(plan.cg, plan.bn, mx, plan.kt, *info, 0, plan.cap, none, none_args, stream, &slots) !=
+            cudaSuccess)
+            return FP4_ERR_CUDA;
+        const int64_t t = tiles % std::max(slots, 1);
+        if (t > 0 && 2 * t <= slots) tail = t;
+    }
+    const size_t tail_ws_bytes = static_cast<size_t>(tail) * plan.cg * plan.bn * kBM * 4;
+    const size_t tail_flag_bytes = static_cast<size_t>(tail) * plan.cg * kEpiWarps * 8;
+    if (tail && ext_scratch && scratch_bytes + tail_ws_bytes + tail_flag_bytes > ext_bytes) tail = 0;
+    const size_t tail_off = scratch_bytes;
+    if (tail) scratch_bytes += tail_ws_bytes + tail_flag_bytes;
     uint8_t *scratch = nullptr;
     if (ext_scratch) {
         if (scratch_bytes > ext_bytes) return FP4_ERR_SCRATCH_LIMIT;
@@ -1037,7 +1147,6 @@ fp4_status gemm_impl(fp4_format fmt, int prepacked, const void *A, const void *s
         }
         const int apk = mx ? 2 : 4;
         const int nrb = static_cast<int>(cdiv(plan.bn, 128));
-        const int64_t k_tiles = cdiv(K, kBK);
         Maps m;
         std::memset(&m, 0, sizeof m);
         if (!encode_operand(&m.a, op_a, rows_a, K, kBM, plan.kt) ||
@@ -1057,7 +1166,14 @@ fp4_status gemm_impl(fp4_format fmt, int prepacked, const void *A, const void *s
         a.splits = static_cast<int32_t>(cdiv(a.k_tiles, a.kps));   // no empty split
         a.tiles_a = static_cast<int32_t>(cdiv(rows_a, kBM * plan.cg));
         a.tiles_b = static_cast<int32_t>(cdiv(rows_b, plan.bn));
-        a.units = a.tiles_a * a.tiles_b * a.splits;
+        a.units = a.tiles_a * a.tiles_b * a.splits + static_cast<int32_t>(tail);
+        a.split_units = static_cast<int32_t>(2 * tail);
+        a.kh = static_cast<int32_t>(k_tiles / 2);
+        if (tail) {
+            a.tail_ws = reinterpret_cast<float *>(scratch + tail_off);
+            a.tail_flags = reinterpret_cast<unsigned long long *>(scratch + tail_off + tail_ws_bytes);
+        }
+        a.epoch = ++g_epoch;
         a.group_b = std::max(1, std::min(a.tiles_b, 8));
         a.bf16 = out == FP4_OUT_BF16;
         a.alpha = alpha;

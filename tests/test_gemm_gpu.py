@@ -263,6 +263,29 @@ def test_deterministic_bytes(fp4, orc):
     np.testing.assert_array_equal(c, d)
 
 
+# The last, partial wave of direct-mode one-CTA tiles runs as two K halves when it
+# fills at most half of the resident CTAs (the caps below force such tails).
+SPLIT_TAIL_CASES = [
+    # fmt, out, M, N, K, (mode, bn, cta_group, max_ctas); one CTA per MMA (pairs do not split)
+    ("nvfp4", "bf16", 768, 768, 1280, (1, 256, 1, 14)),     # 18 tiles on 14 CTAs: 4 split, odd k-tile count
+    ("mxfp4", "f32", 768, 768, 1280, (1, 256, 1, 14)),
+    ("nvfp4", "f32", 512, 1024, 1312, (1, 256, 1, 12)),     # 16 tiles on 12 CTAs: 4 split; K tail
+    ("mxfp4", "bf16", 384, 640, 2048, (1, 256, 1, 6)),      # 9 tiles on 6 CTAs: 3 split; partial tiles
+    ("nvfp4", "f32", 256, 256, 1024, (1, 256, 1, 0)),       # 2 tiles, every CTA free: both split
+    ("nvfp4", "bf16", 384, 640, 2048, (1, 256, 2, 10)),     # a pair: no split (control)
+]
+
+
+@pytest.mark.parametrize("case", SPLIT_TAIL_CASES, ids=lambda c: "%s_%s_%dx%dx%d" % c[:5])
+def test_split_tail(fp4, orc, case):
+    fmt, out, M, N, K, (mode, bn, cg, cap) = case
+    inp = W.make_random(fmt, M, N, K, out=out, alpha=0.5, seed=M + K)
+    cfg = fp4.GemmConfig(mode=mode, bn=bn, cta_group=cg, max_ctas=cap)
+    a = run(fp4, inp, cfg)
+    check_full(orc, inp, a, "split tail %s" % (case,))
+    np.testing.assert_array_equal(a, run(fp4, inp, cfg))      # fixed summation order
+
+
 def test_persistent_grid_cap(fp4, orc):
     # few CTAs, many tiles each: exercises the stage / accumulator phase wrap-around
     inp = W.make_random("nvfp4", 1024, 1024, 1024, out="f32", seed=6)
