@@ -102,7 +102,7 @@ struct Args {
     unsigned long long epoch;            // this launch's flag value
 };
 
-template <int CG, int BN, bool MX, int KT>
+template <int CG, int BN, bool MX>
 struct Cfg {
     static constexpr int APK = MX ? 2 : 4;             // scale atoms per k-tile per 128-row block
     static constexpr int NRB = (BN + 127) / 128;       // 128-row scale blocks on the N side (whole tile)
@@ -113,14 +113,13 @@ struct Cfg {
     static constexpr int SFA_BYTES = APK * kAtomBytes;
     static constexpr int SFB_BYTES = NRB * APK * kAtomBytes;
     static constexpr int KTILE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
-    // a stage is KT consecutive k-tile slots, filled by one TMA load per operand
-    static constexpr int STAGE_BYTES = KT * KTILE_BYTES;
+    static constexpr int STAGE_BYTES = KTILE_BYTES;   // a stage is one k-tile
     static constexpr int BAR_BYTES = 256;
     static constexpr int STAGING_BYTES = kEpiWarps * kStgBytes;     // 8 KB
     static constexpr int BUDGET = kSmemLimit - 1024 - BAR_BYTES - STAGING_BYTES;
     static constexpr int STAGES_FIT = BUDGET / STAGE_BYTES;
-    static constexpr int STAGES = STAGES_FIT * KT > 8 ? 8 / KT : STAGES_FIT;
-    static constexpr int SLOTS = STAGES * KT;                   // k-tile slots in the ring
+    static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
+    static constexpr int SLOTS = STAGES;
     static constexpr int ACC_BUFS = BN <= 128 ? 2 : 1;
     static constexpr int SF_COLS = 4 * APK * (1 + NRB);        // TMEM columns of one k-tile's scales
     static constexpr int SF_TMEM = ACC_BUFS * BN;               // first scale column
@@ -137,7 +136,6 @@ struct Cfg {
     static constexpr int COLS_WARP = BN / 2;                        // accumulator columns per epilogue warp
     static constexpr uint32_t TX_BYTES = CG * STAGE_BYTES;          // bytes landing per stage (both CTAs)
     static_assert(CG == 1 || CG == 2, "CTA group of 1 or 2");
-    static_assert(KT == 1 || KT == 2, "one or two k-tiles per stage");
     static_assert(CG == 1 || BN >= 128, "paired CTAs use N tiles of 128 or 256");
     static_assert(STAGES >= 2, "too few pipeline stages");
     static_assert(TMEM_USED <= 512, "TMEM budget exceeded");
@@ -327,13 +325,13 @@ __device__ __forceinline__ void store_chunk32(uint8_t *stg, const uint32_t (&w)[
     __syncwarp();
 }
 
-template <int CG, int BN, bool MX, int KT>
+template <int CG, int BN, bool MX>
 __global__ void __launch_bounds__(kThreads, 1)
     fp4_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                     const __grid_constant__ CUtensorMap tmap_sfa, const __grid_constant__ CUtensorMap tmap_sfb,
                     const Args args)
 {
-    using C = Cfg<CG, BN, MX, KT>;
+    using C = Cfg<CG, BN, MX>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -402,29 +400,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int row_a = rba * kBM;
                 const int row_b = tb * BN + static_cast<int>(rank) * C::BN_CTA;
                 const int rbb = (tb * BN) / 128;                         // first scale block of the N side
-                for (int kt = kt0; kt < kt1; kt += KT) {
+                for (int kt = kt0; kt < kt1; ++kt) {
                     if (!wait(bar_empty + 8 * stage, phase ^ 1u, args.wait_ns, abort_flag)) {
                         ok = false;
                         break;
                     }
                     const uint32_t full = full0 + 8 * stage;                 // shared::cluster address
                     if (rank == 0) mbar_arrive_expect_tx(bar_full + 8 * stage, C::TX_BYTES);
-                    const int slot = stage * KT;
-                    if constexpr (KT == 1) {
-                        tma_load_2d<CG>(base + C::OFF_A + slot * C::A_BYTES, &tmap_a, full, kt * kBKBytes, row_a);
-                        tma_load_2d<CG>(base + C::OFF_B + slot * C::B_BYTES, &tmap_b, full, kt * kBKBytes, row_b);
-                        tma_load_2d<CG>(base + C::OFF_SFA + slot * C::SFA_BYTES, &tmap_sfa, full,
-                                        kt * C::APK * (kAtomBytes / 8), rba);
-                        tma_load_2d<CG>(base + C::OFF_SFB + slot * C::SFB_BYTES, &tmap_sfb, full,
-                                        kt * C::APK * (kAtomBytes / 8), rbb);
-                    } else {
-                        // 3-D views with the k-tile as the outer coordinate: one load per
-                        // operand fills KT consecutive k-tile slots (past K: zero fill)
-                        tma_load_3d<CG>(base + C::OFF_A + slot * C::A_BYTES, &tmap_a, full, 0, row_a, kt);
-                        tma_load_3d<CG>(base + C::OFF_B + slot * C::B_BYTES, &tmap_b, full, 0, row_b, kt);
-                        tma_load_3d<CG>(base + C::OFF_SFA + slot * C::SFA_BYTES, &tmap_sfa, full, 0, rba, kt);
-                        tma_load_3d<CG>(base + C::OFF_SFB + slot * C::SFB_BYTES, &tmap_sfb, full, 0, rbb, kt);
-                    }
+                    const int slot = stage;
+                    tma_load_2d<CG>(base + C::OFF_A + slot * C::A_BYTES, &tmap_a, full, kt * kBKBytes, row_a);
+                    tma_load_2d<CG>(base + C::OFF_B + slot * C::B_BYTES, &tmap_b, full, kt * kBKBytes, row_b);
+                    tma_load_2d<CG>(base + C::OFF_SFA + slot * C::SFA_BYTES, &tmap_sfa, full,
+                                    kt * C::APK * (kAtomBytes / 8), rba);
+                    tma_load_2d<CG>(base + C::OFF_SFB + slot * C::SFB_BYTES, &tmap_sfb, full,
+                                    kt * C::APK * (kAtomBytes / 8), rbb);
                     filled |= 1u << stage;
                     fill_parity = (fill_parity & ~(1u << stage)) | (phase << stage);
                     if (++stage == C::STAGES) {
@@ -464,7 +453,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // the epilogue has drained this accumulator (once per tile)
                 if (!wait_cluster(bar_acc_empty + 8 * acc, acc_phase ^ 1u, args.wait_ns, abort_flag)) break;
                 const uint32_t d_tmem = tmem + static_cast<uint32_t>(acc * BN);
-                for (int kt = kt0; kt < kt1; kt += KT) {
+                for (int kt = kt0; kt < kt1; ++kt) {
                     // The waiter warp has seen this stage land once its count passes `consumed`.
                     if (ready == consumed) {
                         ready = take_credit(ready_addr, consumed, args.wait_ns, abort_flag);
@@ -474,10 +463,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                     }
                     tc_fence_after();
-#pragma unroll
-                    for (int j = 0; j < KT; ++j) {
-                        if (KT > 1 && kt + j >= kt1) break;              // last stage of an odd k range
-                        const int slot = stage * KT + j;
+                    {
+                        const int slot = stage;
                         const uint32_t sf = tmem + static_cast<uint32_t>(C::SF_TMEM + slot * C::SF_COLS);
                         const uint64_t dsa = desc_sfa0 + static_cast<uint64_t>((slot * C::SFA_BYTES) >> 4);
                         const uint64_t dsb = desc_sfb0 + static_cast<uint64_t>((slot * C::SFB_BYTES) >> 4);
@@ -496,8 +483,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             const int t = MX ? (i >> 1) : i;
                             const uint32_t idesc = (MX && (i & 1)) ? ID2 : ID0;
                             tc_mma_fp4<CG, MX>(d_tmem, da + 2 * i, db + 2 * i, idesc, sf + 4 * t,
-                                               sf + 4 * C::APK + 4 * C::NRB * t,
-                                               (kt + j > kt0 || i > 0) ? 1u : 0u);
+                                               sf + 4 * C::APK + 4 * C::NRB * t, (kt > kt0 || i > 0) ? 1u : 0u);
                         }
                     }
                     tc_commit<CG>(bar_empty + 8 * stage);
@@ -531,7 +517,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int u = pair; ok && u < args.units; u += npairs) {
                 int ta, tb, split, kt0, kt1, half, tidx;
                 unit_work(args, u, ta, tb, split, kt0, kt1, half, tidx);
-                for (int kt = kt0; kt < kt1; kt += KT) {
+                for (int kt = kt0; kt < kt1; ++kt) {
                     if (!wait(bar_full + 8 * stage, phase, args.wait_ns, abort_flag)) {
                         ok = false;
                         break;
@@ -740,7 +726,7 @@ int64_t g_wait_ms = -1;
 std::atomic<unsigned long long> g_epoch{0};   // per-launch value of the split-tail flags
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
-constexpr int kNumKernels = 20;   // kernel variants that can be launched (see kernel_index)
+constexpr int kNumKernels = 14;   // kernel variants that can be launched (see kernel_index)
 struct DeviceInfo {
     bool probed = false;
     bool ok = false;
@@ -797,45 +783,25 @@ bool encode(CUtensorMap *m, CUtensorMapDataType dt, int rank, const void *ptr, c
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Operand map: rows x K/2 bytes, box of `box_rows` rows x one 128-byte k-tile
-// (2-D), or, with kt == 2, a 3-D view (byte in k-tile, row, k-tile) whose box
-// covers two consecutive k-tiles. 128-byte swizzle.
-bool encode_operand(CUtensorMap *m, const void *ptr, int64_t rows, int64_t K, int box_rows, int kt)
+// Operand map: rows x K/2 bytes, box of `box_rows` rows x one 128-byte k-tile,
+// 128-byte swizzle.
+bool encode_operand(CUtensorMap *m, const void *ptr, int64_t rows, int64_t K, int box_rows)
 {
-    if (kt == 1) {
-        const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K / 2), static_cast<cuuint64_t>(rows)};
-        const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K / 2)};
-        const cuuint32_t box[2] = {static_cast<cuuint32_t>(kBKBytes), static_cast<cuuint32_t>(box_rows)};
-        return encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, ptr, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
-    }
-    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kBKBytes), static_cast<cuuint64_t>(rows),
-                                static_cast<cuuint64_t>(K / kBK)};
-    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(K / 2), static_cast<cuuint64_t>(kBKBytes)};
-    const cuuint32_t box[3] = {static_cast<cuuint32_t>(kBKBytes), static_cast<cuuint32_t>(box_rows),
-                               static_cast<cuuint32_t>(kt)};
-    return encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, ptr, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K / 2), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K / 2)};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(kBKBytes), static_cast<cuuint32_t>(box_rows)};
+    return encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, ptr, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 // Scale-atom map: the atom buffer as int64 rows of ceil(K/vec/4) * 64 elements
-// per 128-row block; a box is one k-tile's atoms of `box_blocks` blocks (2-D),
-// or, with kt == 2, a 3-D view (element in k-tile, block, k-tile) covering two
-// k-tiles. Past the matrix the box is zero-filled.
-bool encode_scales(CUtensorMap *m, const void *atoms, int64_t row_blocks, int64_t kc4, int apk, int box_blocks,
-                   int kt, int64_t k_tiles)
+// per 128-row block; a box is one k-tile's atoms of `box_blocks` blocks. Past the
+// matrix the box is zero-filled.
+bool encode_scales(CUtensorMap *m, const void *atoms, int64_t row_blocks, int64_t kc4, int apk, int box_blocks)
 {
-    if (kt == 1) {
-        const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kc4 * 64), static_cast<cuuint64_t>(row_blocks)};
-        const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kc4 * kAtomBytes)};
-        const cuuint32_t box[2] = {static_cast<cuuint32_t>(apk * 64), static_cast<cuuint32_t>(box_blocks)};
-        return encode(m, CU_TENSOR_MAP_DATA_TYPE_INT64, 2, atoms, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
-    }
-    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(apk * 64), static_cast<cuuint64_t>(row_blocks),
-                                static_cast<cuuint64_t>(k_tiles)};
-    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(kc4 * kAtomBytes),
-                                   static_cast<cuuint64_t>(apk * kAtomBytes)};
-    const cuuint32_t box[3] = {static_cast<cuuint32_t>(apk * 64), static_cast<cuuint32_t>(box_blocks),
-                               static_cast<cuuint32_t>(kt)};
-    return encode(m, CU_TENSOR_MAP_DATA_TYPE_INT64, 3, atoms, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kc4 * 64), static_cast<cuuint64_t>(row_blocks)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kc4 * kAtomBytes)};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(apk * 64), static_cast<cuuint32_t>(box_blocks)};
+    return encode(m, CU_TENSOR_MAP_DATA_TYPE_INT64, 2, atoms, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -857,14 +823,14 @@ struct Maps {
     CUtensorMap a, b, sfa, sfb;
 };
 
-template <int CG, int BN, bool MX, int KT>
 // With `slots_out` set, only reports how many CTA groups a launch can keep
 // resident (after the cap) and launches nothing.
+template <int CG, int BN, bool MX>
 cudaError_t launch_gemm(DeviceInfo &info, int kidx, int units, int cap, const Maps &m, const Args &args,
                         cudaStream_t stream, int *slots_out)
 {
-    using C = Cfg<CG, BN, MX, KT>;
-    auto kern = fp4_gemm_kernel<CG, BN, MX, KT>;
+    using C = Cfg<CG, BN, MX>;
+    auto kern = fp4_gemm_kernel<CG, BN, MX>;
     cudaLaunchAttribute cluster_attr[1];
     cluster_attr[0].id = cudaLaunchAttributeClusterDimension;
     cluster_attr[0].val.clusterDim.x = CG;
@@ -911,50 +877,42 @@ cudaError_t launch_gemm(DeviceInfo &info, int kidx, int units, int cap, const Ma
     return cudaLaunchKernelEx(&lc, kern, m.a, m.b, m.sfa, m.sfb, args);
 }
 
-// Variants: one CTA: N 16..256, pair: N 128 / 256; each for both formats, with
-// one k-tile per stage; pairs with MXFP4 also with two k-tiles per stage.
-int kernel_index(int cg, int bn, bool mx, int kt)
+// Variants: one CTA: N 16..256, pair: N 128 / 256; each for both formats.
+int kernel_index(int cg, int bn, bool mx)
 {
     if (cg == 1) return bn_index(bn) * 2 + (mx ? 1 : 0);                   // 0..9
-    const int w = bn == 256 ? 1 : 0;
-    if (kt == 1) return 10 + w * 2 + (mx ? 1 : 0);                          // 10..13
-    return 14 + w;                                                          // 14..15 (MXFP4)
+    return 10 + (bn == 256 ? 2 : 0) + (mx ? 1 : 0);                         // 10..13
 }
 
-cudaError_t launch_by_cfg(int cg, int bn, bool mx, int kt, DeviceInfo &info, int units, int cap, const Maps &m,
+cudaError_t launch_by_cfg(int cg, int bn, bool mx, DeviceInfo &info, int units, int cap, const Maps &m,
                           const Args &args, cudaStream_t stream, int *slots_out = nullptr)
 {
-    const int k = kernel_index(cg, bn, mx, kt);
-#define FP4_LAUNCH(CG_, BN_, MX_, KT_) \
-    return launch_gemm<CG_, BN_, MX_, KT_>(info, k, units, cap, m, args, stream, slots_out)
+    const int k = kernel_index(cg, bn, mx);
+#define FP4_LAUNCH(CG_, BN_, MX_) return launch_gemm<CG_, BN_, MX_>(info, k, units, cap, m, args, stream, slots_out)
     if (cg == 2) {
-        if (kt == 2) {
-            if (bn == 256) FP4_LAUNCH(2, 256, true, 2);
-            FP4_LAUNCH(2, 128, true, 2);
-        }
         if (bn == 256) {
-            if (mx) FP4_LAUNCH(2, 256, true, 1);
-            FP4_LAUNCH(2, 256, false, 1);
+            if (mx) FP4_LAUNCH(2, 256, true);
+            FP4_LAUNCH(2, 256, false);
         }
-        if (mx) FP4_LAUNCH(2, 128, true, 1);
-        FP4_LAUNCH(2, 128, false, 1);
+        if (mx) FP4_LAUNCH(2, 128, true);
+        FP4_LAUNCH(2, 128, false);
     }
     switch (bn) {
     case 16:
-        if (mx) FP4_LAUNCH(1, 16, true, 1);
-        FP4_LAUNCH(1, 16, false, 1);
+        if (mx) FP4_LAUNCH(1, 16, true);
+        FP4_LAUNCH(1, 16, false);
     case 32:
-        if (mx) FP4_LAUNCH(1, 32, true, 1);
-        FP4_LAUNCH(1, 32, false, 1);
+        if (mx) FP4_LAUNCH(1, 32, true);
+        FP4_LAUNCH(1, 32, false);
     case 64:
-        if (mx) FP4_LAUNCH(1, 64, true, 1);
-        FP4_LAUNCH(1, 64, false, 1);
+        if (mx) FP4_LAUNCH(1, 64, true);
+        FP4_LAUNCH(1, 64, false);
     case 128:
-        if (mx) FP4_LAUNCH(1, 128, true, 1);
-        FP4_LAUNCH(1, 128, false, 1);
+        if (mx) FP4_LAUNCH(1, 128, true);
+        FP4_LAUNCH(1, 128, false);
     default:
-        if (mx) FP4_LAUNCH(1, 256, true, 1);
-        FP4_LAUNCH(1, 256, false, 1);
+        if (mx) FP4_LAUNCH(1, 256, true);
+        FP4_LAUNCH(1, 256, false);
     }
 #undef FP4_LAUNCH
 }
@@ -963,7 +921,6 @@ struct Plan {
     bool swap;
     int bn;
     int cg;
-    int kt;         // k-tiles per pipeline stage
     int splits;
     int cap;
 };
@@ -1034,9 +991,6 @@ fp4_status make_plan(int64_t M, int64_t N, int64_t K, bool rows_ok, bool mx, int
     }
     p.splits = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(splits, k_tiles)));
     p.cap = (cfg && cfg->max_ctas > 0) ? cfg->max_ctas : 0;
-    // Two k-tiles per TMA load where the producer would otherwise limit the MMA
-    // rate (MXFP4 pairs); the 3-D views need whole k-tiles (K % 256 == 0).
-    p.kt = (mx && cg == 2 && K % kBK == 0) ? 2 : 1;
     return FP4_OK;
 }
 
@@ -1115,8 +1069,7 @@ fp4_status gemm_impl(fp4_format fmt, int prepacked, const void *A, const void *s
         Args none_args;
         std::memset(&none, 0, sizeof none);
         std::memset(&none_args, 0, sizeof none_args);
-        if (launch_by_cfg(plan.cg, plan.bn, mx, plan.kt, *info, 0, plan.cap, none, none_args, stream, &slots) !=
-            cudaSuccess)
+        if (launch_by_cfg(plan.cg, plan.bn, mx, *info, 0, plan.cap, none, none_args, stream, &slots) != cudaSuccess)
             return FP4_ERR_CUDA;
         const int64_t t = tiles % std::max(slots, 1);
         if (t > 0 && 2 * t <= slots) tail = t;
@@ -1149,10 +1102,9 @@ fp4_status gemm_impl(fp4_format fmt, int prepacked, const void *A, const void *s
         const int nrb = static_cast<int>(cdiv(plan.bn, 128));
         Maps m;
         std::memset(&m, 0, sizeof m);
-        if (!encode_operand(&m.a, op_a, rows_a, K, kBM, plan.kt) ||
-            !encode_operand(&m.b, op_b, rows_b, K, plan.bn / plan.cg, plan.kt) ||
-            !encode_scales(&m.sfa, sfa_atoms, rb_a, kc4, apk, 1, plan.kt, k_tiles) ||
-            !encode_scales(&m.sfb, sfb_atoms, rb_b, kc4, apk, nrb, plan.kt, k_tiles)) {
+        if (!encode_operand(&m.a, op_a, rows_a, K, kBM) || !encode_operand(&m.b, op_b, rows_b, K, plan.bn / plan.cg) ||
+            !encode_scales(&m.sfa, sfa_atoms, rb_a, kc4, apk, 1) ||
+            !encode_scales(&m.sfb, sfb_atoms, rb_b, kc4, apk, nrb)) {
             result = FP4_ERR_CUDA;
             break;
         }
@@ -1191,7 +1143,7 @@ fp4_status gemm_impl(fp4_format fmt, int prepacked, const void *A, const void *s
             a.out = D;
             a.ldo = N;
         }
-        if (launch_by_cfg(plan.cg, plan.bn, mx, plan.kt, *info, a.units, plan.cap, m, a, stream) != cudaSuccess) {
+        if (launch_by_cfg(plan.cg, plan.bn, mx, *info, a.units, plan.cap, m, a, stream) != cudaSuccess) {
             result = FP4_ERR_CUDA;
             break;
         }

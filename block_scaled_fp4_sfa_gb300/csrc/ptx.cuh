@@ -22,13 +22,6 @@ __device__ __forceinline__ uint64_t global_timer_ns()
     return t;
 }
 
-__device__ __forceinline__ uint32_t lane_id()
-{
-    uint32_t l;
-    asm volatile("mov.u32 %0, %%laneid;" : "=r"(l));
-    return l;
-}
-
 // ---- mbarrier ----------------------------------------------------------------
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
@@ -66,7 +59,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
     return ok != 0;
 }
 
-// ---- proxies and named barriers ----------------------------------------------
+// ---- acquire / release ---------------------------------------------------------
 
 // try_wait with acquire semantics at cluster scope (for barriers that threads
 // of the peer CTA arrive on with release.cluster).
@@ -107,31 +100,6 @@ __device__ __forceinline__ void st_release_gpu_u64(unsigned long long *p, unsign
     asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
 
-__device__ __forceinline__ void fence_proxy_async_smem()
-{
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
-__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads)
-{
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
-}
-
-// Named-barrier AND-reduction: every participating thread gets the AND of `v`.
-__device__ __forceinline__ bool named_bar_and(uint32_t id, uint32_t nthreads, bool v)
-{
-    uint32_t out;
-    asm volatile(
-        "{\n\t.reg .pred pi, po;\n\t"
-        "setp.ne.u32 pi, %3, 0;\n\t"
-        "bar.red.and.pred po, %1, %2, pi;\n\t"
-        "selp.u32 %0, 1, 0, po;\n\t}"
-        : "=r"(out)
-        : "r"(id), "r"(nthreads), "r"(static_cast<uint32_t>(v))
-        : "memory");
-    return out != 0;
-}
-
 // ---- TMA / bulk copies ---------------------------------------------------------
 
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map)
@@ -160,44 +128,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
     }
 }
 
-// 3-D tiled TMA load (same completion and CTA-pair rules as tma_load_2d).
-template <int CG>
-__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, uint32_t bar, int32_t x,
-                                            int32_t y, int32_t z)
-{
-    if constexpr (CG == 2) {
-        asm volatile(
-            "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
-            " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
-            "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "r"(z)
-            : "memory");
-    } else {
-        asm volatile(
-            "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-            " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
-            "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "r"(z)
-            : "memory");
-    }
-}
-
-// Same, with an L2 eviction-priority hint (a createpolicy value).
-__device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap *map, uint32_t bar,
-                                                 int32_t x, int32_t y, uint64_t policy)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
-        " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "l"(policy)
-        : "memory");
-}
-
-__device__ __forceinline__ uint64_t policy_evict_last()
-{
-    uint64_t p;
-    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
-    return p;
-}
-
 __device__ __forceinline__ uint64_t policy_evict_first()
 {
     uint64_t p;
@@ -221,43 +151,6 @@ __device__ __forceinline__ void st_global_b32_hint(void *p, uint32_t v, uint64_t
 __device__ __forceinline__ void st_global_b16_hint(void *p, uint16_t v, uint64_t policy)
 {
     asm volatile("st.global.L2::cache_hint.b16 [%0], %1, %2;" ::"l"(p), "h"(v), "l"(policy) : "memory");
-}
-
-// Contiguous global -> shared bulk copy (16-byte aligned addresses, size % 16 == 0).
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar)
-{
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
-        : "memory");
-}
-
-// 2-D tiled TMA store from shared memory (bulk-group completion).
-__device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, uint32_t src, int32_t x, int32_t y)
-{
-    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
-                     reinterpret_cast<uint64_t>(map)),
-                 "r"(src), "r"(x), "r"(y)
-                 : "memory");
-}
-
-__device__ __forceinline__ void bulk_commit_group()
-{
-    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-}
-
-// Wait until at most N bulk groups still read their shared-memory source.
-template <int N>
-__device__ __forceinline__ void bulk_wait_group_read()
-{
-    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
-}
-
-// Wait until at most N bulk groups are still in flight (writes done).
-template <int N>
-__device__ __forceinline__ void bulk_wait_group()
-{
-    asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
 }
 
 // ---- tcgen05: tensor memory ------------------------------------------------------

@@ -237,9 +237,8 @@ def test_k_tail_not_multiple_of_tile(fp4, orc):
 
 
 @pytest.mark.parametrize("K", [256, 768, 1280, 1792])
-def test_two_ktile_stages(fp4, orc, K):
-    # MXFP4 CTA pairs load two k-tiles per TMA box when K % 256 == 0; odd k-tile
-    # counts and split-K ranges end on a half-used stage
+def test_mxfp4_pairs_k_lengths(fp4, orc, K):
+    # CTA pairs over odd and even k-tile counts, direct and split-K
     inp = W.make_random("mxfp4", 520, 384, K, out="bf16", seed=K)
     check_full(orc, inp, run(fp4, inp, fp4.GemmConfig(mode=1, bn=256, cta_group=2)), "direct K=%d" % K)
     check_full(orc, inp, run(fp4, inp, fp4.GemmConfig(mode=1, bn=128, cta_group=2)), "direct bn128 K=%d" % K)
