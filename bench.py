@@ -79,25 +79,30 @@ def peaks():
         return FALLBACK_BF16_TFLOPS, FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_source_hash():
+GEMM_SOURCES = ("block_scaled_fp4_sfa_gb300/csrc/fp4_gemm.cu", "block_scaled_fp4_sfa_gb300/csrc/ptx.cuh")
+QUANT_SOURCES = ("block_scaled_fp4_sfa_gb300/csrc/fp4_quant.cu",)
+
+
+def kernel_source_hash(sources=GEMM_SOURCES):
     h = hashlib.sha256()
-    for rel in ("block_scaled_fp4_sfa_gb300/csrc/fp4_gemm.cu", "block_scaled_fp4_sfa_gb300/csrc/ptx.cuh"):
+    for rel in sources:
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(workload):
-    """DRAM bytes per GEMM launch from the committed ncu summary, if it was taken
-    on the current kernel source (else None)."""
-    path = os.path.join(ROOT, "profiles", "gemm_traffic.json")
+def ncu_traffic(workload, sources=GEMM_SOURCES):
+    """DRAM bytes per launch of the workload's kernel from the committed ncu
+    summary (profiles/traffic.json), if it was taken on the current kernel
+    source (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
             t = json.load(f)
     except (OSError, ValueError):
         return None
     e = t.get(workload)
-    if not e or e.get("kernel_hash") != kernel_source_hash():
+    if not e or e.get("kernel_hash") != kernel_source_hash(sources):
         return None
     return float(e["dram_bytes_per_launch"])
 
@@ -316,18 +321,28 @@ def run_ours(args, inp, rank, ws, local):
     fp4_peak = bf16_peak * FP4_PER_BF16
     traffic = ncu_traffic(inp.name)
     alg_bytes = (inp.M + inp.N) * (inp.K // 2 + inp.K // vec) + inp.M * inp.N * (4 if inp.out == "f32" else 2)
+    # the binding roof: HBM when the arithmetic intensity is below the ridge
+    # (skinny shapes), else the FP4 tensor rate
+    hbm_bound = inp.flops / alg_bytes < fp4_peak * 1e12 / (hbm_peak * 1e9)
+    achieved_gbs = alg_bytes / (gemm_avg_ms * 1e-3) / 1e9
+    if hbm_bound:
+        roofline = {"bound": "hbm", "achieved": achieved_gbs, "peak": hbm_peak, "unit": "GB/s",
+                    "frac": achieved_gbs / hbm_peak, "traffic": traffic,
+                    "peak_source": "%s HBM copy bandwidth" % peak_src,
+                    "tensor_tflops": achieved, "tensor_frac": achieved / fp4_peak}
+    else:
+        roofline = {"bound": "tensor", "achieved": achieved, "peak": fp4_peak, "unit": "TFLOP/s",
+                    "frac": achieved / fp4_peak, "traffic": traffic,
+                    "peak_source": "%s bf16 burst %.1f TFLOP/s x %.0f (nominal FP4:bf16)" % (
+                        peak_src, bf16_peak, FP4_PER_BF16)}
+    roofline.update({"kernel": "fp4_gemm_kernel", "gemm_us": 1e3 * gemm_avg_ms, "algorithmic_bytes": alg_bytes,
+                     "hbm_frac_at_algorithmic_bytes": achieved_gbs / hbm_peak})
     result = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "e2m1", "data": "synthetic",
         "config": dict(workload_config(inp), parallelism="replicas" if ws > 1 else "single"),
-        "roofline": {"bound": "tensor", "achieved": achieved, "peak": fp4_peak, "unit": "TFLOP/s",
-                     "frac": achieved / fp4_peak, "traffic": traffic,
-                     "peak_source": "%s bf16 burst %.1f TFLOP/s x %.0f (nominal FP4:bf16)" % (peak_src, bf16_peak,
-                                                                                            FP4_PER_BF16),
-                     "kernel": "fp4_gemm_kernel", "gemm_us": 1e3 * gemm_avg_ms,
-                     "algorithmic_bytes": alg_bytes,
-                     "hbm_frac_at_algorithmic_bytes": alg_bytes / (gemm_avg_ms * 1e-3) / 1e9 / hbm_peak},
+        "roofline": roofline,
         "e2e": {"value": inp.flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": 3 * args.steps,
@@ -426,7 +441,7 @@ def run_quant(args, rank, ws, local):
     achieved = nbytes / (avg_ms * 1e-3) / 1e9
     res.update({
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
-                     "frac": achieved / hbm_peak, "traffic": None,
+                     "frac": achieved / hbm_peak, "traffic": ncu_traffic(name, QUANT_SOURCES),
                      "peak_source": "%s HBM copy bandwidth" % peak_src, "kernel": "quantize_kernel",
                      "kernel_us": 1e3 * avg_ms, "algorithmic_bytes": nbytes},
         "e2e": {"value": nbytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
@@ -441,13 +456,18 @@ def run_quant(args, rank, ws, local):
         oracle.quantize(X[:n], fmt)
         dt = time.perf_counter() - t0
         n = int(max(1, min(rows, n * args.cpu_sample_s / 4 / max(dt, 1e-6))))
-        t0 = time.perf_counter()
-        oracle.quantize(X[:n], fmt)
-        dt = time.perf_counter() - t0
-        res["cpu_baseline"] = {"value": quant_bytes(n, K, vec, X.itemsize, 0) / dt / 1e9, "unit": "GB/s",
+        # whole passes over the sample until about cpu_sample_s / 2 seconds have run
+        reps, t0 = 0, time.perf_counter()
+        while True:
+            oracle.quantize(X[:n], fmt)
+            reps += 1
+            dt = time.perf_counter() - t0
+            if dt >= args.cpu_sample_s / 2 or reps >= 1000:
+                break
+        res["cpu_baseline"] = {"value": reps * quant_bytes(n, K, vec, X.itemsize, 0) / dt / 1e9, "unit": "GB/s",
                                "cores": os.cpu_count(), "kind": "oracle",
-                               "sample": "first %d of %d rows of %s, %.1f s, C oracle (fp32 decisions), plain scales"
-                                         % (n, rows, name, dt)}
+                               "sample": "first %d of %d rows of %s, %d passes, %.1f s, C oracle (fp32 decisions), "
+                                         "plain scales" % (n, rows, name, reps, dt)}
     return res
 
 
