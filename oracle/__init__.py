@@ -12,6 +12,8 @@ Functions (each follows the passage cited in ``oracle.c``):
 * ``round_bf16(x)`` -> uint16 bf16 bits (one rounding, ties to even).
 * ``scale_reorder(sf, rows, ksf)`` -> the 128x4 atom layout (uint8).
 * ``e2m1_encode(q)``, ``e4m3_encode(v)`` -> nearest code (ties to the even code).
+* ``epilogue(y, bias, op)`` -> bias, then none / ReLU / squared ReLU / SwiGLU
+  (interleaved gate, up columns) on fp64 GEMM results.
 * ``quantize(X, fmt)`` -> (packed E2M1 codes, plain row-major scale bytes) of
   fp32 or bf16 values, one scale per 16 (nvfp4) or 32 (mxfp4) values.
 
@@ -87,6 +89,8 @@ def _load():
         lib.oracle_quantize.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_int64,
                                         ctypes.c_int, _u8p, _u8p]
         lib.oracle_quantize.restype = ctypes.c_int
+        lib.oracle_epilogue.argtypes = [_f64p, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p, ctypes.c_int, _f64p]
+        lib.oracle_epilogue.restype = ctypes.c_int
         _lib = lib
     return _lib
 
@@ -201,3 +205,21 @@ def quantize(X: np.ndarray, fmt: str) -> tuple[np.ndarray, np.ndarray]:
     if rc != 0:
         raise ValueError("oracle_quantize rejected its arguments")
     return codes, sf
+
+
+EPILOGUE_OPS = {"none": 0, "relu": 1, "relu2": 2, "swiglu": 3}
+
+
+def epilogue(y: np.ndarray, bias, op: str) -> np.ndarray:
+    """y: [rows][N] fp64 (alpha already applied); bias: float32 [N] or None.
+    Returns [rows][N] (or [rows][N/2] for swiglu) fp64, before output rounding."""
+    y = np.ascontiguousarray(y, dtype=np.float64)
+    rows, N = y.shape
+    code = EPILOGUE_OPS[op]
+    out = np.empty((rows, N // 2 if code == 3 else N), dtype=np.float64)
+    b = None if bias is None else np.ascontiguousarray(bias, dtype=np.float32)
+    rc = _load().oracle_epilogue(_ptr(y, _f64p), rows, N, None if b is None else b.ctypes.data, code,
+                                 _ptr(out, _f64p))
+    if rc != 0:
+        raise ValueError("oracle_epilogue rejected its arguments")
+    return out

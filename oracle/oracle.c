@@ -333,3 +333,42 @@ int oracle_quantize(const void *X, int in_bf16, int64_t rows, int64_t K, int vec
     }
     return 0;
 }
+
+/* ---- fused epilogues --------------------------------------------------------- */
+/*
+ * Applied to the GEMM's unrounded result y[m][n] = alpha * sum_k a_k b_k (the
+ * rows of oracle_gemm_rows): z = y + bias[n] (bias may be NULL), then
+ *   op 0: z;  op 1: max(z, 0);  op 2: max(z, 0)^2 (squared ReLU);
+ *   op 3: SwiGLU over interleaved columns, out[m][j] = silu(z[m][2j]) * z[m][2j+1]
+ *         with silu(x) = x / (1 + exp(-x)), for j < N/2.
+ * The pages list these as the elementwise work around the GEMM ("TMA Pipelines,
+ * Tensor Cores, and ctm-rs Interop", "Where to Go Next": SwiGLU elementwise;
+ * the NVFP4 ReLU^2 MoE). Reading: bias before the activation; the gate is the
+ * even column of each pair. fp64 throughout (exp from the C library).
+ * out has rows x N (ops 0-2) or rows x N/2 (op 3) entries. Returns 0, or -1.
+ */
+int oracle_epilogue(const double *y, int64_t rows, int64_t N, const float *bias, int op, double *out)
+{
+    if (rows < 0 || N < 0 || op < 0 || op > 3) return -1;
+    if (op == 3 && N % 2 != 0) return -1;
+    for (int64_t m = 0; m < rows; ++m) {
+        if (op == 3) {
+            for (int64_t j = 0; j < N / 2; ++j) {
+                double g = y[m * N + 2 * j], u = y[m * N + 2 * j + 1];
+                if (bias) {
+                    g += (double)bias[2 * j];
+                    u += (double)bias[2 * j + 1];
+                }
+                out[m * (N / 2) + j] = g / (1.0 + exp(-g)) * u;
+            }
+            continue;
+        }
+        for (int64_t n = 0; n < N; ++n) {
+            double z = y[m * N + n] + (bias ? (double)bias[n] : 0.0);
+            if (op >= 1 && z < 0.0) z = 0.0;
+            if (op == 2) z = z * z;
+            out[m * N + n] = z;
+        }
+    }
+    return 0;
+}

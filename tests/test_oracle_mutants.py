@@ -37,6 +37,14 @@ MUTANTS = {
     "reorder_atoms_row_major_by_k": ("(r / 128) * kc4 + c / 4", "(c / 4) * ((rows + 127) / 128) + r / 128"),
 }
 
+EPILOGUE_MUTANTS = {
+    "swiglu_gate_up_swapped": ("out[m * (N / 2) + j] = g / (1.0 + exp(-g)) * u;", "out[m * (N / 2) + j] = u / (1.0 + exp(-u)) * g;"),
+    "silu_sign_flipped": ("g / (1.0 + exp(-g)) * u", "g / (1.0 + exp(g)) * u"),
+    "relu2_without_clamp": ("if (op >= 1 && z < 0.0) z = 0.0;", "if (op == 1 && z < 0.0) z = 0.0;"),
+    "bias_dropped": ("double z = y[m * N + n] + (bias ? (double)bias[n] : 0.0);", "double z = y[m * N + n];"),
+    "swiglu_bias_on_up_only": ("g += (double)bias[2 * j];", "g += 0.0;"),
+}
+
 QUANT_MUTANTS = {
     "e2m1_ties_to_odd": ("if (dc < db || (dc == db && c % 2 == 0)) best = c;\n    }\n    return sign | best;",
                          "if (dc < db || (dc == db && c % 2 == 1)) best = c;\n    }\n    return sign | best;"),
@@ -74,6 +82,12 @@ def _run_mutant(old, new, pins, tmp_path):
 @pytest.mark.parametrize("name", sorted(MUTANTS))
 def test_pins_reject_mutant(name, tmp_path):
     r = _run_mutant(*MUTANTS[name], "test_oracle.py", tmp_path)
+    assert r.returncode != 0, "mutant %s survived the pins:\n%s" % (name, r.stdout[-2000:])
+
+
+@pytest.mark.parametrize("name", sorted(EPILOGUE_MUTANTS))
+def test_epilogue_pins_reject_mutant(name, tmp_path):
+    r = _run_mutant(*EPILOGUE_MUTANTS[name], "test_oracle_epilogue.py", tmp_path)
     assert r.returncode != 0, "mutant %s survived the pins:\n%s" % (name, r.stdout[-2000:])
 
 
