@@ -24,6 +24,12 @@ own GPU with no collective in the data path (weak scaling).
 --impl reference times the CPU oracle (the only reference this project has)
 on the same workload, one bounded row sample per step.
 
+--op fused times the GEMM with a fused epilogue (fp4_gemm_fused: bias,
+ReLU, squared ReLU or SwiGLU applied to the accumulator before the cast) on
+the FFN workloads ffn_*; same metric, roofline and legs, with the oracle's
+GEMM plus its epilogue as the cpu_baseline and e2e through pinned host
+buffers copied on the stream around the same call.
+
 --op quantize measures the quantisation step that feeds the GEMM instead
 (fp4_quantize: bf16 or fp32 activations -> E2M1 codes + atom-layout scales),
 against the HBM roofline: its bytes (values read, codes and scale atoms
@@ -51,6 +57,7 @@ import workloads as W  # noqa: E402
 
 METRIC = "block-scaled FP4 GEMM TFLOP/s on 1 GB300 and % of dense FP4 tensor peak"
 DEFAULT_WORKLOAD = "nvfp4_4096_bf16"
+DEFAULT_FUSED_WORKLOAD = "ffn_swiglu_nvfp4_m8192_n28672_k4096"
 FP4_PER_BF16 = 13.5 / 2.25       # nominal dense FP4 : dense bf16 tensor throughput on GB300
 FALLBACK_BF16_TFLOPS = 1900.0
 FALLBACK_HBM_GBS = 6800.0
@@ -160,10 +167,12 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-def oracle_rows_tflops(inp, rows, nthreads=0):
+def oracle_rows_tflops(inp, rows, nthreads=0, act=None, bias=None):
     import oracle
     t0 = time.perf_counter()
-    oracle.gemm_rows(inp, rows, nthreads=nthreads)
+    y, _ = oracle.gemm_rows(inp, rows, nthreads=nthreads)
+    if act is not None:
+        oracle.epilogue(y, bias, act)
     dt = time.perf_counter() - t0
     return 2.0 * len(rows) * inp.N * inp.K / dt / 1e12, dt
 
@@ -215,12 +224,16 @@ def whole_job_tflops(flops_per_step, steps, world_size, total_ms):
     return flops_per_step * steps * world_size / (total_ms * 1e-3) / 1e12
 
 
-def workload_config(inp):
-    return {"workload": inp.name, "format": inp.fmt, "M": inp.M, "N": inp.N, "K": inp.K, "out": inp.out,
-            "alpha": inp.alpha, "l2": "flushed between steps (256 MiB write, outside the step events)"}
+def workload_config(inp, act=None, bias=None):
+    c = {"workload": inp.name, "format": inp.fmt, "M": inp.M, "N": inp.N, "K": inp.K, "out": inp.out,
+         "alpha": inp.alpha, "l2": "flushed between steps (256 MiB write, outside the step events)"}
+    if act is not None:
+        c["epilogue"] = act
+        c["bias"] = bias is not None
+    return c
 
 
-def run_ours(args, inp, rank, ws, local):
+def run_ours(args, inp, rank, ws, local, act=None, bias=None):
     import torch
     import block_scaled_fp4_sfa_gb300 as fp4
 
@@ -234,10 +247,21 @@ def run_ours(args, inp, rank, ws, local):
     atomA = torch.empty(fp4.scale_atom_bytes(inp.M, inp.K, vec), dtype=torch.uint8, device=dev)
     atomB = torch.empty(fp4.scale_atom_bytes(inp.N, inp.K, vec), dtype=torch.uint8, device=dev)
     odt = torch.float32 if inp.out == "f32" else torch.bfloat16
-    D = torch.empty(inp.M, inp.N, dtype=odt, device=dev)
+    fused = act is not None
+    d_cols = inp.N // 2 if act == "swiglu" else inp.N
+    D = torch.empty(inp.M, d_cols, dtype=odt, device=dev)
+    hbias = torch.from_numpy(bias) if bias is not None else None
+    dbias = hbias.to(dev) if bias is not None else None
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     prepacked = fp4.gemm_nvfp4_prepacked if inp.fmt == "nvfp4" else fp4.gemm_mxfp4_prepacked
     s = stream.cuda_stream
+
+    def gemm_call(a, sa, b, sb, d, bb):
+        if fused:
+            fp4.gemm_fused(inp.fmt, a, sa, b, sb, inp.alpha, d, inp.M, inp.N, inp.K, inp.out, act=act, bias=bb,
+                           prepacked=True, stream=s)
+        else:
+            prepacked(a, sa, b, sb, inp.alpha, d, inp.M, inp.N, inp.K, inp.out, stream=s)
 
     def spacer():
         # a spin kernel keeps the GPU busy while the host enqueues the step, so no
@@ -248,7 +272,7 @@ def run_ours(args, inp, rank, ws, local):
         fp4.scale_reorder(sfA, atomA, inp.M, inp.K, vec, stream=s)
         fp4.scale_reorder(sfB, atomB, inp.N, inp.K, vec, stream=s)
         ev_g0.record(stream)
-        prepacked(A, atomA, B, atomB, inp.alpha, D, inp.M, inp.N, inp.K, inp.out, stream=s)
+        gemm_call(A, atomA, B, atomB, D, dbias)
         ev_g1.record(stream)
 
     ev_g0 = torch.cuda.Event(enable_timing=True)
@@ -293,26 +317,41 @@ def run_ours(args, inp, rank, ws, local):
     value = whole_job_tflops(inp.flops, args.steps, ws, total_ms)
 
     result_quick = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "ms_per_step": ms_per_step,
-                    "gemm_us": 1e3 * sum(gemm_ms) / len(gemm_ms), "config": workload_config(inp)}
+                    "gemm_us": 1e3 * sum(gemm_ms) / len(gemm_ms), "config": workload_config(inp, act, bias)}
     if args.quick:
         return result_quick
 
-    # e2e: host buffers through fp4_gemm_host, pinned memory, copies inside the timed region
+    # e2e: host buffers, pinned memory, copies inside the timed region -- through
+    # fp4_gemm_host, or for a fused epilogue the same copies on the stream around
+    # fp4_gemm_fused (plain scales: it reorders them itself)
     pA, psA, pB, psB = (t.pin_memory() for t in (hA, hsA, hB, hsB))
-    pD = torch.empty(inp.M, inp.N, dtype=odt).pin_memory()
+    pD = torch.empty(inp.M, d_cols, dtype=odt).pin_memory()
+    pbias = hbias.pin_memory() if hbias is not None else None
+
+    def e2e_step():
+        if not fused:
+            fp4.gemm_host(inp.fmt, pA, psA, pB, psB, inp.alpha, pD, inp.M, inp.N, inp.K, inp.out, stream=s)
+            return
+        for dst, src in ((A, pA), (sfA, psA), (B, pB), (sfB, psB), (dbias, pbias)):
+            if dst is not None:
+                dst.copy_(src, non_blocking=True)
+        fp4.gemm_fused(inp.fmt, A, sfA, B, sfB, inp.alpha, D, inp.M, inp.N, inp.K, inp.out, act=act, bias=dbias,
+                       stream=s)
+        pD.copy_(D, non_blocking=True)
+
     e_steps = max(3, min(args.steps, 20))
     for _ in range(2):
-        fp4.gemm_host(inp.fmt, pA, psA, pB, psB, inp.alpha, pD, inp.M, inp.N, inp.K, inp.out, stream=s)
+        e2e_step()
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(e_steps):
-        fp4.gemm_host(inp.fmt, pA, psA, pB, psB, inp.alpha, pD, inp.M, inp.N, inp.K, inp.out, stream=s)
+        e2e_step()
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / e_steps
-    h2d = sum(t.numel() * t.element_size() for t in (hA, hsA, hB, hsB))
+    h2d = sum(t.numel() * t.element_size() for t in (hA, hsA, hB, hsB) + ((hbias,) if hbias is not None else ()))
     d2h = pD.numel() * pD.element_size()
 
     bf16_peak, hbm_peak, peak_src = peaks()
@@ -320,7 +359,8 @@ def run_ours(args, inp, rank, ws, local):
     achieved = inp.flops / (gemm_avg_ms * 1e-3) / 1e12
     fp4_peak = bf16_peak * FP4_PER_BF16
     traffic = ncu_traffic(inp.name)
-    alg_bytes = (inp.M + inp.N) * (inp.K // 2 + inp.K // vec) + inp.M * inp.N * (4 if inp.out == "f32" else 2)
+    alg_bytes = ((inp.M + inp.N) * (inp.K // 2 + inp.K // vec) + inp.M * d_cols * (4 if inp.out == "f32" else 2)
+                 + (4 * inp.N if bias is not None else 0))
     # the binding roof: HBM when the arithmetic intensity is below the ridge
     # (skinny shapes), else the FP4 tensor rate
     hbm_bound = inp.flops / alg_bytes < fp4_peak * 1e12 / (hbm_peak * 1e9)
@@ -341,7 +381,7 @@ def run_ours(args, inp, rank, ws, local):
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "e2m1", "data": "synthetic",
-        "config": dict(workload_config(inp), parallelism="replicas" if ws > 1 else "single"),
+        "config": dict(workload_config(inp, act, bias), parallelism="replicas" if ws > 1 else "single"),
         "roofline": roofline,
         "e2e": {"value": inp.flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
@@ -477,8 +517,9 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--op", choices=["gemm", "quantize"], default="gemm")
-    ap.add_argument("--workload", default=None, choices=W.config_names() + sorted(W.QUANT_WORKLOADS))
+    ap.add_argument("--op", choices=["gemm", "fused", "quantize"], default="gemm")
+    ap.add_argument("--workload", default=None,
+                    choices=W.config_names() + sorted(W.FUSED_WORKLOADS) + sorted(W.QUANT_WORKLOADS))
     ap.add_argument("--cpu-sample-s", type=float, default=12.0, help="oracle seconds for cpu_baseline")
     ap.add_argument("--ref-step-s", type=float, default=3.0, help="oracle seconds per reference step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -490,13 +531,16 @@ def main():
         ap.error("--warmup must be >= 3")
     ws, rank, local = dist_env()
     if args.workload is None:
-        args.workload = DEFAULT_QUANT_WORKLOAD if args.op == "quantize" else DEFAULT_WORKLOAD
-    if (args.op == "quantize") != (args.workload in W.QUANT_WORKLOADS):
+        args.workload = {"quantize": DEFAULT_QUANT_WORKLOAD, "fused": DEFAULT_FUSED_WORKLOAD}.get(
+            args.op, DEFAULT_WORKLOAD)
+    table = {"quantize": W.QUANT_WORKLOADS, "fused": W.FUSED_WORKLOADS}.get(args.op)
+    valid = table if table is not None else W.config_names()
+    if args.workload not in valid:
         ap.error("--op %s does not take workload %s" % (args.op, args.workload))
+    if args.op != "gemm" and args.impl == "reference":
+        ap.error("--impl reference times the GEMM's oracle; use --op gemm")
 
     if args.op == "quantize":
-        if args.impl == "reference":
-            ap.error("--impl reference times the GEMM's oracle; use --op gemm")
         if ws > 1:
             import torch
             torch.cuda.set_device(local)
@@ -515,14 +559,19 @@ def main():
             import torch
             torch.cuda.set_device(local)
             torch.distributed.init_process_group("nccl")
-        inp = W.make_config(args.workload)
-        res = run_ours(args, inp, rank, ws, local)
+        act = bias = None
+        if args.op == "fused":
+            inp, act, bias = W.make_fused(args.workload)
+        else:
+            inp = W.make_config(args.workload)
+        res = run_ours(args, inp, rank, ws, local, act, bias)
         if rank == 0 and not args.no_cpu_baseline and not args.quick:
             rows = cpu_sample_rows(inp, args.cpu_sample_s)
-            v, dt = oracle_rows_tflops(inp, rows)
+            v, dt = oracle_rows_tflops(inp, rows, act=act, bias=bias)
+            what = "fp64 C oracle" + (" + its %s epilogue" % act if act else "")
             res["cpu_baseline"] = {"value": v, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
-                                   "sample": "%d of %d rows of %s (all %d columns), %.1f s, fp64 C oracle"
-                                             % (len(rows), inp.M, inp.name, inp.N, dt)}
+                                   "sample": "%d of %d rows of %s (all %d columns), %.1f s, %s"
+                                             % (len(rows), inp.M, inp.name, inp.N, dt, what)}
         if ws > 1:
             import torch
             torch.distributed.destroy_process_group()

@@ -20,7 +20,7 @@ from . import _build
 __all__ = ["FP4_OK", "Fp4Error", "load", "build", "gemm", "gemm_nvfp4", "gemm_mxfp4", "gemm_nvfp4_prepacked",
            "gemm_mxfp4_prepacked", "gemm_host", "scale_reorder", "scale_atom_bytes", "get_device_status",
            "status_string", "set_wait_limit_ms", "GemmConfig", "FMT", "OUT", "gemm_static_scratch",
-           "STATIC_SCRATCH_BYTES", "quantize", "IN", "SF_LAYOUT"]
+           "STATIC_SCRATCH_BYTES", "quantize", "IN", "SF_LAYOUT", "gemm_fused", "ACT", "Epilogue"]
 
 FP4_OK = 0
 STATUS_NAMES = {0: "FP4_OK", 1: "FP4_ERR_INVALID_ARG", 2: "FP4_ERR_UNSUPPORTED", 3: "FP4_ERR_MISALIGNED",
@@ -30,6 +30,7 @@ FMT = {"nvfp4": 0, "mxfp4": 1}
 OUT = {"f32": 0, "bf16": 1}
 IN = {"f32": 0, "bf16": 1}
 SF_LAYOUT = {"plain": 0, "atom": 1}
+ACT = {"none": 0, "relu": 1, "relu2": 2, "swiglu": 3}
 
 _lib = None
 
@@ -44,6 +45,11 @@ class GemmConfig(ctypes.Structure):
     """fp4_gemm_config: plan overrides (0 = automatic)."""
     _fields_ = [("mode", ctypes.c_int32), ("bn", ctypes.c_int32), ("splits", ctypes.c_int32),
                 ("max_ctas", ctypes.c_int32), ("cta_group", ctypes.c_int32)]
+
+
+class Epilogue(ctypes.Structure):
+    """fp4_epilogue: activation code and an optional device bias pointer."""
+    _fields_ = [("act", ctypes.c_int32), ("bias", ctypes.c_void_p)]
 
 
 def build(force: bool = False) -> str:
@@ -67,6 +73,9 @@ def load():
     lib.fp4_gemm.argtypes = [i32, i32, vp, vp, vp, vp, f32, vp, i64, i64, i64, i32,
                              ctypes.POINTER(GemmConfig), vp]
     lib.fp4_gemm.restype = i32
+    lib.fp4_gemm_fused.argtypes = [i32, i32, vp, vp, vp, vp, f32, ctypes.POINTER(Epilogue), vp, i64, i64, i64, i32,
+                                   ctypes.POINTER(GemmConfig), vp]
+    lib.fp4_gemm_fused.restype = i32
     lib.fp4_gemm_host.argtypes = [i32, vp, vp, vp, vp, f32, vp, i64, i64, i64, i32, vp]
     lib.fp4_gemm_host.restype = i32
     lib.fp4_gemm_static_scratch.argtypes = [i32, vp, vp, vp, vp, f32, vp, i64, i64, i64, i32, vp]
@@ -125,6 +134,20 @@ def gemm(fmt: str, A, sfA, B, sfB, alpha: float, D, M: int, N: int, K: int, out:
                          _ptr(D), int(M), int(N), int(K), OUT[out], cfg, _stream(stream))
     if check:
         _check(st, "fp4_gemm")
+    return st
+
+
+def gemm_fused(fmt: str, A, sfA, B, sfB, alpha: float, D, M: int, N: int, K: int, out: str = "f32", *,
+               act: str = "none", bias=None, prepacked: bool = False, config: GemmConfig | None = None,
+               stream=None, check: bool = True) -> int:
+    """fp4_gemm_fused: D = act(alpha * decode(A, sfA) . decode(B, sfB)^T + bias). D has N / 2 columns
+    for act="swiglu" (gate and up columns interleaved in B)."""
+    epi = Epilogue(ACT[act], _ptr(bias))
+    cfg = ctypes.byref(config) if config is not None else None
+    st = load().fp4_gemm_fused(FMT[fmt], int(bool(prepacked)), _ptr(A), _ptr(sfA), _ptr(B), _ptr(sfB), float(alpha),
+                               ctypes.byref(epi), _ptr(D), int(M), int(N), int(K), OUT[out], cfg, _stream(stream))
+    if check:
+        _check(st, "fp4_gemm_fused")
     return st
 
 

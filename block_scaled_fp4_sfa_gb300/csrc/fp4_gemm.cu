@@ -89,7 +89,9 @@ struct Args {
     int32_t tiles_a, tiles_b, splits, units, group_b;
     int32_t bf16;            // output type for modes 0 and 1
     int32_t mode;            // EpiMode
+    int32_t act;             // fp4_activation (modes 0 and 1; split-K partials stay raw)
     float alpha;
+    const float *bias;       // NULL, or one float per GEMM output column (modes 0 and 1)
     // Split tail (direct mode): units 0 .. split_units-1 are the two K halves of
     // the first split_units / 2 tiles (the tiles beyond the last full wave, run
     // first so that their extra epilogue work overlaps later tiles). The first
@@ -298,6 +300,20 @@ __device__ __forceinline__ void tmem_load_cols(uint32_t taddr, uint32_t *v)
             tmem_ld_32x32b_x32(taddr + 32 * c, r);
         }
     }
+}
+
+__device__ __forceinline__ float silu(float x) { return x / (1.0f + expf(-x)); }
+
+// The fused epilogue on one element: ReLU or squared ReLU (SwiGLU pairs two
+// elements and is done by the callers).
+__device__ __forceinline__ float activate(float z, int act)
+{
+    if (act == FP4_ACT_RELU) return fmaxf(z, 0.0f);
+    if (act == FP4_ACT_RELU2) {
+        const float r = fmaxf(z, 0.0f);
+        return r * r;
+    }
+    return z;
 }
 
 // One warp stores a 32-row x 32-byte chunk of D: lane l holds row row0 + l's
@@ -590,32 +606,84 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int row_base = (ta * CG + static_cast<int>(rank)) * kBM + 32 * q;   // this warp's first row
                 const int ra = row_base + lane;                                            // slot-A row of this lane
                 const int col0 = tb * BN + h * C::COLS_WARP;                                // first slot-B row
+                const bool glu = args.act == FP4_ACT_SWIGLU;
+                if (args.mode != kEpiSplitK) {
+                    // z = alpha * acc + bias, then the activation. Rows mode: v[i] is
+                    // GEMM column col0 + i; transposed: every v[i] of this lane is
+                    // GEMM column ra.
+                    if (args.bias) {
+                        if (args.mode == kEpiRows) {
+#pragma unroll
+                            for (int i = 0; i < C::COLS_WARP; ++i) {
+                                const float b = col0 + i < args.rows_b ? __ldg(args.bias + col0 + i) : 0.0f;
+                                v[i] = __float_as_uint(fmaf(__uint_as_float(v[i]), args.alpha, b));
+                            }
+                        } else {
+                            const float b = ra < args.rows_a ? __ldg(args.bias + ra) : 0.0f;
+#pragma unroll
+                            for (int i = 0; i < C::COLS_WARP; ++i)
+                                v[i] = __float_as_uint(fmaf(__uint_as_float(v[i]), args.alpha, b));
+                        }
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < C::COLS_WARP; ++i)
+                            v[i] = __float_as_uint(__uint_as_float(v[i]) * args.alpha);
+                    }
+                    if (glu) {
+                        if (args.mode == kEpiRows) {
+                            // gate = even column, up = odd column: pack the N/2 results
+                            // into v[0 .. COLS_WARP/2)
+#pragma unroll
+                            for (int j = 0; j < C::COLS_WARP / 2; ++j)
+                                v[j] = __float_as_uint(silu(__uint_as_float(v[2 * j])) *
+                                                       __uint_as_float(v[2 * j + 1]));
+                        } else {
+                            // gate on the even lane, up on the odd lane next to it
+#pragma unroll
+                            for (int i = 0; i < C::COLS_WARP; ++i) {
+                                const float z = __uint_as_float(v[i]);
+                                const float up = __shfl_xor_sync(0xFFFFFFFFu, z, 1);
+                                v[i] = __float_as_uint(silu(z) * up);
+                            }
+                        }
+                    } else if (args.act != FP4_ACT_NONE) {
+#pragma unroll
+                        for (int i = 0; i < C::COLS_WARP; ++i)
+                            v[i] = __float_as_uint(activate(__uint_as_float(v[i]), args.act));
+                    }
+                }
                 if (args.mode == kEpiRows || ra < args.rows_a) {       // the row stores are warp-collective
                     if (args.mode == kEpiRows) {
-                        // D rows of this warp in 32-byte column chunks through the staging
+                        // D rows of this warp in 32-byte column chunks through the staging;
+                        // SwiGLU stores half as many columns, from D column col0 / 2
+                        const int oc0 = glu ? col0 >> 1 : col0;
+                        const int ocols = glu ? args.rows_b >> 1 : args.rows_b;
+                        const int nval = glu ? C::COLS_WARP / 2 : C::COLS_WARP;
                         if (args.bf16) {
 #pragma unroll
                             for (int ch = 0; ch < C::COLS_WARP / 16; ++ch) {
-                                uint32_t w[8];
+                                if (16 * ch < nval) {
+                                    uint32_t w[8];
 #pragma unroll
-                                for (int i = 0; i < 8; ++i) {
-                                    __nv_bfloat162 p = __floats2bfloat162_rn(
-                                        __uint_as_float(v[16 * ch + 2 * i]) * args.alpha,
-                                        __uint_as_float(v[16 * ch + 2 * i + 1]) * args.alpha);
-                                    w[i] = *reinterpret_cast<uint32_t *>(&p);
+                                    for (int i = 0; i < 8; ++i) {
+                                        __nv_bfloat162 p = __floats2bfloat162_rn(__uint_as_float(v[16 * ch + 2 * i]),
+                                                                                 __uint_as_float(v[16 * ch + 2 * i + 1]));
+                                        w[i] = *reinterpret_cast<uint32_t *>(&p);
+                                    }
+                                    store_chunk32(stg_ptr, w, args.out, args.ldo, 2, row_base, oc0 + 16 * ch, 8,
+                                                  args.rows_a, ocols, lane, d_policy);
                                 }
-                                store_chunk32(stg_ptr, w, args.out, args.ldo, 2, row_base, col0 + 16 * ch, 8,
-                                              args.rows_a, args.rows_b, lane, d_policy);
                             }
                         } else {
 #pragma unroll
                             for (int ch = 0; ch < C::COLS_WARP / 8; ++ch) {
-                                uint32_t w[8];
+                                if (8 * ch < nval) {
+                                    uint32_t w[8];
 #pragma unroll
-                                for (int i = 0; i < 8; ++i)
-                                    w[i] = __float_as_uint(__uint_as_float(v[8 * ch + i]) * args.alpha);
-                                store_chunk32(stg_ptr, w, args.out, args.ldo, 4, row_base, col0 + 8 * ch, 4,
-                                              args.rows_a, args.rows_b, lane, d_policy);
+                                    for (int i = 0; i < 8; ++i) w[i] = v[8 * ch + i];
+                                    store_chunk32(stg_ptr, w, args.out, args.ldo, 4, row_base, oc0 + 8 * ch, 4,
+                                                  args.rows_a, ocols, lane, d_policy);
+                                }
                             }
                         }
                     } else if (args.mode == kEpiSplitK) {
@@ -626,22 +694,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int i = 0; i < C::COLS_WARP; ++i)
                             if (col0 + i < args.rows_b)
                                 st_global_b32_hint(ws + static_cast<int64_t>(col0 + i) * args.ldo, v[i], d_policy);
-                    } else if (args.bf16) {
-                        __nv_bfloat16 *d = static_cast<__nv_bfloat16 *>(args.out) + ra;
+                    } else if (!glu || (lane & 1) == 0) {
+                        // D^T: this lane's GEMM column ra (SwiGLU: D column ra / 2, from the gate lane)
+                        const int oc = glu ? ra >> 1 : ra;
+                        if (args.bf16) {
+                            __nv_bfloat16 *d = static_cast<__nv_bfloat16 *>(args.out) + oc;
 #pragma unroll
-                        for (int i = 0; i < C::COLS_WARP; ++i)
-                            if (col0 + i < args.rows_b)
-                                st_global_b16_hint(
-                                    d + static_cast<int64_t>(col0 + i) * args.ldo,
-                                    __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v[i]) * args.alpha)),
-                                    d_policy);
-                    } else {
-                        float *d = static_cast<float *>(args.out) + ra;
+                            for (int i = 0; i < C::COLS_WARP; ++i)
+                                if (col0 + i < args.rows_b)
+                                    st_global_b16_hint(d + static_cast<int64_t>(col0 + i) * args.ldo,
+                                                       __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v[i]))),
+                                                       d_policy);
+                        } else {
+                            float *d = static_cast<float *>(args.out) + oc;
 #pragma unroll
-                        for (int i = 0; i < C::COLS_WARP; ++i)
-                            if (col0 + i < args.rows_b)
-                                st_global_b32_hint(d + static_cast<int64_t>(col0 + i) * args.ldo,
-                                                   __float_as_uint(__uint_as_float(v[i]) * args.alpha), d_policy);
+                            for (int i = 0; i < C::COLS_WARP; ++i)
+                                if (col0 + i < args.rows_b)
+                                    st_global_b32_hint(d + static_cast<int64_t>(col0 + i) * args.ldo, v[i], d_policy);
+                        }
                     }
                 }
             }
@@ -661,22 +731,39 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 1) tmem_dealloc<CG>(tmem, C::TMEM_COLS);
 }
 
-// Split-K: D[rb][ra] = alpha * sum_s ws[s][rb][ra] (fixed order, deterministic).
+// Split-K: z[rb][ra] = alpha * sum_s ws[s][rb][ra] (+ bias[ra]) in a fixed
+// order (deterministic), then the fused epilogue into D[rb][.]. With splits = 0
+// (K = 0) z is the bias alone.
+__device__ __forceinline__ float splitk_z(const float *__restrict__ ws, int64_t at, int splits, int64_t split_stride,
+                                          float alpha, const float *__restrict__ bias, int64_t ra)
+{
+    float s = 0.f;
+    for (int k = 0; k < splits; ++k) s += ws[k * split_stride + at];
+    return bias ? fmaf(s, alpha, bias[ra]) : s * alpha;
+}
+
 __global__ void splitk_reduce_kernel(const float *__restrict__ ws, void *__restrict__ out, int64_t rows_b,
                                      int64_t rows_a, int64_t ldd, int splits, int64_t split_stride, float alpha,
-                                     int bf16)
+                                     int bf16, const float *__restrict__ bias, int act)
 {
-    const int64_t total = rows_b * rows_a;
+    const bool glu = act == FP4_ACT_SWIGLU;
+    const int64_t cols = glu ? rows_a / 2 : rows_a;   // D columns
+    const int64_t total = rows_b * cols;
     for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
          i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        const int64_t rb = i / rows_a, ra = i - rb * rows_a;
-        float s = 0.f;
-        for (int k = 0; k < splits; ++k) s += ws[k * split_stride + rb * rows_a + ra];
-        s *= alpha;
+        const int64_t rb = i / cols, c = i - rb * cols;
+        float r;
+        if (glu) {
+            const float g = splitk_z(ws, rb * rows_a + 2 * c, splits, split_stride, alpha, bias, 2 * c);
+            const float u = splitk_z(ws, rb * rows_a + 2 * c + 1, splits, split_stride, alpha, bias, 2 * c + 1);
+            r = silu(g) * u;
+        } else {
+            r = activate(splitk_z(ws, rb * rows_a + c, splits, split_stride, alpha, bias, c), act);
+        }
         if (bf16)
-            static_cast<__nv_bfloat16 *>(out)[rb * ldd + ra] = __float2bfloat16_rn(s);
+            static_cast<__nv_bfloat16 *>(out)[rb * ldd + c] = __float2bfloat16_rn(r);
         else
-            static_cast<float *>(out)[rb * ldd + ra] = s;
+            static_cast<float *>(out)[rb * ldd + c] = r;
     }
 }
 
@@ -1012,18 +1099,37 @@ fp4_status reorder_launch(const void *sf_plain, void *sf_atom, int64_t rows, int
 fp4_status gemm_impl(fp4_format fmt, int prepacked, const void *A, const void *sfA, const void *B,
                      const void *sfB, float alpha, void *D, int64_t M, int64_t N, int64_t K, fp4_out_dtype out,
                      const fp4_gemm_config *cfg, cudaStream_t stream, uint8_t *ext_scratch = nullptr,
-                     size_t ext_bytes = 0)
+                     size_t ext_bytes = 0, const fp4_epilogue *epi = nullptr)
 {
     if (fmt != FP4_FMT_NVFP4 && fmt != FP4_FMT_MXFP4) return FP4_ERR_INVALID_ARG;
     if (out != FP4_OUT_F32 && out != FP4_OUT_BF16) return FP4_ERR_INVALID_ARG;
+    const int act = epi ? epi->act : FP4_ACT_NONE;
+    const float *bias = epi ? epi->bias : nullptr;
+    if (act < FP4_ACT_NONE || act > FP4_ACT_SWIGLU) return FP4_ERR_INVALID_ARG;
     if (M < 0 || N < 0 || K < 0) return FP4_ERR_INVALID_ARG;
+    const bool glu = act == FP4_ACT_SWIGLU;
+    if (glu && N % 2 != 0) return FP4_ERR_UNSUPPORTED;
     if (M == 0 || N == 0) return FP4_OK;
     if (!D) return FP4_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(bias) & 3u) return FP4_ERR_MISALIGNED;
     const int64_t esize = out == FP4_OUT_BF16 ? 2 : 4;
+    const int64_t d_cols = glu ? N / 2 : N;          // columns of D
     if (K == 0) {
         if (!aligned16(D)) return FP4_ERR_MISALIGNED;
-        return cudaMemsetAsync(D, 0, static_cast<size_t>(M * N * esize), stream) == cudaSuccess ? FP4_OK
-                                                                                              : FP4_ERR_CUDA;
+        if (act == FP4_ACT_NONE && !bias)
+            return cudaMemsetAsync(D, 0, static_cast<size_t>(M * d_cols * esize), stream) == cudaSuccess
+                       ? FP4_OK
+                       : FP4_ERR_CUDA;
+        if (M > (1ll << 30) || N > (1ll << 30) || M * N > (1ll << 46)) return FP4_ERR_UNSUPPORTED;
+        int dev;
+        DeviceInfo *info;
+        fp4_status st = device_info(dev, info);
+        if (st != FP4_OK) return st;
+        // D = epilogue(bias): the split-K reduce with no partials
+        const int64_t blocks = std::min<int64_t>(cdiv(M * d_cols, 256), static_cast<int64_t>(info->sms) * 8);
+        splitk_reduce_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+            nullptr, D, M, N, d_cols, 0, 0, alpha, out == FP4_OUT_BF16, bias, act);
+        return cudaGetLastError() == cudaSuccess ? FP4_OK : FP4_ERR_CUDA;
     }
     if (!A || !B || !sfA || !sfB) return FP4_ERR_INVALID_ARG;
     if (K % 32 != 0) return FP4_ERR_UNSUPPORTED;
@@ -1041,7 +1147,7 @@ fp4_status gemm_impl(fp4_format fmt, int prepacked, const void *A, const void *s
     const int vec = mx ? 32 : 16;
     const int64_t ksf = K / vec;
     const int64_t kc4 = cdiv(ksf, 4);
-    const bool rows_ok = (N * esize) % 16 == 0;
+    const bool rows_ok = (d_cols * esize) % 16 == 0;
     Plan plan;
     st = make_plan(M, N, K, rows_ok, mx, info->sms, cfg, plan);
     if (st != FP4_OK) return st;
@@ -1129,10 +1235,12 @@ fp4_status gemm_impl(fp4_format fmt, int prepacked, const void *A, const void *s
         a.group_b = std::max(1, std::min(a.tiles_b, 8));
         a.bf16 = out == FP4_OUT_BF16;
         a.alpha = alpha;
+        a.act = act;
+        a.bias = bias;
         if (!plan.swap) {
             a.mode = kEpiRows;
             a.out = D;
-            a.ldo = N;
+            a.ldo = d_cols;
         } else if (a.splits > 1) {
             a.mode = kEpiSplitK;
             a.out = ws;
@@ -1141,7 +1249,7 @@ fp4_status gemm_impl(fp4_format fmt, int prepacked, const void *A, const void *s
         } else {
             a.mode = kEpiTransposed;
             a.out = D;
-            a.ldo = N;
+            a.ldo = d_cols;
         }
         if (launch_by_cfg(plan.cg, plan.bn, mx, *info, a.units, plan.cap, m, a, stream) != cudaSuccess) {
             result = FP4_ERR_CUDA;
@@ -1151,7 +1259,8 @@ fp4_status gemm_impl(fp4_format fmt, int prepacked, const void *A, const void *s
             const int64_t total = rows_a * rows_b;
             const int64_t blocks = std::min<int64_t>(cdiv(total, 256), static_cast<int64_t>(info->sms) * 8);
             splitk_reduce_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
-                reinterpret_cast<const float *>(ws), D, rows_b, rows_a, N, a.splits, a.split_stride, alpha, a.bf16);
+                reinterpret_cast<const float *>(ws), D, rows_b, rows_a, d_cols, a.splits, a.split_stride, alpha,
+                a.bf16, bias, act);
             if (cudaGetLastError() != cudaSuccess) {
                 result = FP4_ERR_CUDA;
                 break;
@@ -1193,6 +1302,13 @@ fp4_status fp4_gemm(fp4_format fmt, int scales_prepacked, const void *A, const v
                     const fp4_gemm_config *cfg, cudaStream_t stream)
 {
     return gemm_impl(fmt, scales_prepacked, A, sfA, B, sfB, alpha, D, M, N, K, out, cfg, stream);
+}
+
+fp4_status fp4_gemm_fused(fp4_format fmt, int scales_prepacked, const void *A, const void *sfA, const void *B,
+                          const void *sfB, float alpha, const fp4_epilogue *epi, void *D, int64_t M, int64_t N,
+                          int64_t K, fp4_out_dtype out, const fp4_gemm_config *cfg, cudaStream_t stream)
+{
+    return gemm_impl(fmt, scales_prepacked, A, sfA, B, sfB, alpha, D, M, N, K, out, cfg, stream, nullptr, 0, epi);
 }
 
 fp4_status fp4_gemm_nvfp4(const void *A, const void *sfA, const void *B, const void *sfB, float alpha, void *D,

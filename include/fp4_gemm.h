@@ -113,6 +113,44 @@ fp4_status fp4_gemm(fp4_format fmt, int scales_prepacked, const void *A, const v
                     const void *B, const void *sfB, float alpha, void *D, int64_t M, int64_t N,
                     int64_t K, fp4_out_dtype out, const fp4_gemm_config *cfg, cudaStream_t stream);
 
+/* Fused epilogue of fp4_gemm_fused, applied to each element of the fp32
+ * accumulator before the output cast (the pages name these elementwise
+ * stages beside their block-scaled GEMMs: "TMA Pipelines, Tensor Cores, and
+ * ctm-rs Interop", section "Where to Go Next" -- the SwiGLU elementwise
+ * workload and the NVFP4 ReLU-squared MoE):
+ *   z[m][n] = alpha * acc[m][n] + (bias ? bias[n] : 0)
+ *   FP4_ACT_NONE    D[m][n] = z[m][n]
+ *   FP4_ACT_RELU    D[m][n] = max(z[m][n], 0)
+ *   FP4_ACT_RELU2   D[m][n] = max(z[m][n], 0)^2
+ *   FP4_ACT_SWIGLU  D[m][j] = silu(z[m][2j]) * z[m][2j+1],  silu(x) = x / (1 + exp(-x)),
+ *                   j < N/2: gate and up projections interleaved column by column
+ *                   in B (gate rows 2j, up rows 2j+1), so D has N/2 columns.
+ * The pages do not fix the SwiGLU column layout; interleaving keeps each
+ * gate/up pair inside one accumulator tile. Arithmetic is fp32 (fmaf for z,
+ * expf and an IEEE division for silu).
+ *   bias: device, N floats (one per GEMM output column, before the SwiGLU
+ *         pairing), 4-byte aligned; NULL for none. Owned by the caller.     */
+typedef enum {
+    FP4_ACT_NONE = 0,
+    FP4_ACT_RELU = 1,
+    FP4_ACT_RELU2 = 2,
+    FP4_ACT_SWIGLU = 3
+} fp4_activation;
+
+typedef struct {
+    int32_t act;          /* fp4_activation */
+    const float *bias;    /* NULL or N floats on the device */
+} fp4_epilogue;
+
+/* fp4_gemm with a fused epilogue (epi may be NULL: then identical to fp4_gemm).
+ * D is [M][N] (fp32 or bf16), or [M][N/2] for FP4_ACT_SWIGLU, which needs N even
+ * (else FP4_ERR_UNSUPPORTED). A misaligned bias gives FP4_ERR_MISALIGNED, an
+ * unknown act FP4_ERR_INVALID_ARG. K == 0 writes the epilogue of z = bias. */
+fp4_status fp4_gemm_fused(fp4_format fmt, int scales_prepacked, const void *A, const void *sfA,
+                          const void *B, const void *sfB, float alpha, const fp4_epilogue *epi,
+                          void *D, int64_t M, int64_t N, int64_t K, fp4_out_dtype out,
+                          const fp4_gemm_config *cfg, cudaStream_t stream);
+
 /* Host-buffer convenience form: A, sfA, B, sfB and D live in HOST memory
  * (pinned for asynchronous copies). The call copies the inputs to stream-ordered
  * device scratch, runs fp4_gemm, copies D back and returns; D is valid once

@@ -98,6 +98,24 @@ def test_host_validation_without_device(fp4):
     assert lib.fp4_gemm_host(0, p, p, p, p, 1.0, p, 64, 64, 40, 0, 0) == 2
 
 
+def test_fused_host_validation_without_device(fp4):
+    buf = np.zeros(4096 + 16, np.uint8)
+    p = buf.ctypes.data + (-buf.ctypes.data) % 16
+    lib = fp4.load()
+
+    def f(act, bias, M, N, K=64):
+        epi = fp4.Epilogue(act, bias)
+        return lib.fp4_gemm_fused(0, 0, p, p, p, p, 1.0, ctypes.byref(epi), p, M, N, K, 0, None, 0)
+
+    assert f(0, None, 0, 64) == 0                  # empty
+    assert f(3, None, 64, 0) == 0
+    assert f(4, None, 64, 64) == 1                 # unknown activation
+    assert f(-1, None, 64, 64) == 1
+    assert f(3, None, 64, 63) == 2                 # SwiGLU needs N even
+    assert f(1, p + 2, 64, 64) == 3                # bias not 4-byte aligned
+    assert f(2, p, 64, 64, K=48) == 2              # K % 32 != 0
+
+
 def test_quantize_host_validation_without_device(fp4):
     buf = np.zeros(4096 + 16, np.uint8)
     p = buf.ctypes.data + (-buf.ctypes.data) % 16

@@ -231,6 +231,37 @@ def make_config(name: str, seed: int = 0) -> GemmInputs:
     return make_random(fmt, M, N, K, dist="normal", alpha=alpha, out=out, seed=seed, name=name)
 
 
+# ---- GEMMs with a fused epilogue ------------------------------------------------
+#
+# FFN projections whose epilogue is fused into the GEMM: the gate/up projection
+# of a SwiGLU FFN (d_model 4096 -> 2 x 14336, gate and up weight rows
+# interleaved, so D is 8192 x 14336) and a squared-ReLU up projection with a
+# bias. Operands as the nvfp4_proj_* workloads (activations N(0, 1), weights
+# N(0, 0.02^2), quantised blockwise); the bias is N(0, 0.5^2) in fp32.
+
+FUSED_WORKLOADS = {
+    "ffn_swiglu_nvfp4_m8192_n28672_k4096": dict(fmt="nvfp4", M=8192, N=28672, K=4096, out="bf16",
+                                                act="swiglu", bias=False),
+    "ffn_relu2_bias_nvfp4_m8192_n14336_k4096": dict(fmt="nvfp4", M=8192, N=14336, K=4096, out="bf16",
+                                                    act="relu2", bias=True),
+}
+
+
+def make_bias(N: int, *, std: float = 0.5, seed: int = 0) -> np.ndarray:
+    """N fp32 bias values, N(0, std^2)."""
+    rng = np.random.default_rng(1000 + seed)
+    return (rng.standard_normal(N) * std).astype(np.float32)
+
+
+def make_fused(name: str, seed: int = 0):
+    """(GemmInputs, act, bias or None) of a named fused-epilogue workload."""
+    w = FUSED_WORKLOADS[name]
+    inp = make_random(w["fmt"], w["M"], w["N"], w["K"], dist="normal", a_std=1.0, b_std=0.02, alpha=1.0,
+                      out=w["out"], seed=seed, name=name)
+    bias = make_bias(w["N"], seed=seed) if w["bias"] else None
+    return inp, w["act"], bias
+
+
 # ---- raw values for the quantisation step -------------------------------------
 #
 # The quantiser's inputs are plain activations: seeded draws rounded to the
