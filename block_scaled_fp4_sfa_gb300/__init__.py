@@ -20,7 +20,7 @@ from . import _build
 __all__ = ["FP4_OK", "Fp4Error", "load", "build", "gemm", "gemm_nvfp4", "gemm_mxfp4", "gemm_nvfp4_prepacked",
            "gemm_mxfp4_prepacked", "gemm_host", "scale_reorder", "scale_atom_bytes", "get_device_status",
            "status_string", "set_wait_limit_ms", "GemmConfig", "FMT", "OUT", "gemm_static_scratch",
-           "STATIC_SCRATCH_BYTES", "quantize", "IN", "SF_LAYOUT", "gemm_fused", "ACT", "Epilogue"]
+           "STATIC_SCRATCH_BYTES", "quantize", "IN", "SF_LAYOUT", "gemm_fused", "ACT", "Epilogue", "gemm_plan", "PlanInfo"]
 
 FP4_OK = 0
 STATUS_NAMES = {0: "FP4_OK", 1: "FP4_ERR_INVALID_ARG", 2: "FP4_ERR_UNSUPPORTED", 3: "FP4_ERR_MISALIGNED",
@@ -52,6 +52,12 @@ class Epilogue(ctypes.Structure):
     _fields_ = [("act", ctypes.c_int32), ("bias", ctypes.c_void_p)]
 
 
+class PlanInfo(ctypes.Structure):
+    """fp4_plan_info: what a call would launch."""
+    _fields_ = [("kernel", ctypes.c_int32), ("swap", ctypes.c_int32), ("bn", ctypes.c_int32),
+                ("cta_group", ctypes.c_int32), ("splits", ctypes.c_int32), ("launches", ctypes.c_int32)]
+
+
 def build(force: bool = False) -> str:
     return _build.build(force=force)
 
@@ -76,6 +82,9 @@ def load():
     lib.fp4_gemm_fused.argtypes = [i32, i32, vp, vp, vp, vp, f32, ctypes.POINTER(Epilogue), vp, i64, i64, i64, i32,
                                    ctypes.POINTER(GemmConfig), vp]
     lib.fp4_gemm_fused.restype = i32
+    lib.fp4_gemm_plan.argtypes = [i32, i32, i64, i64, i64, i32, i32, ctypes.POINTER(GemmConfig),
+                                  ctypes.POINTER(PlanInfo)]
+    lib.fp4_gemm_plan.restype = i32
     lib.fp4_gemm_host.argtypes = [i32, vp, vp, vp, vp, f32, vp, i64, i64, i64, i32, vp]
     lib.fp4_gemm_host.restype = i32
     lib.fp4_gemm_static_scratch.argtypes = [i32, vp, vp, vp, vp, f32, vp, i64, i64, i64, i32, vp]
@@ -149,6 +158,17 @@ def gemm_fused(fmt: str, A, sfA, B, sfB, alpha: float, D, M: int, N: int, K: int
     if check:
         _check(st, "fp4_gemm_fused")
     return st
+
+
+def gemm_plan(fmt: str, M: int, N: int, K: int, out: str = "f32", *, act: str = "none", prepacked: bool = False,
+              config: GemmConfig | None = None) -> dict:
+    """fp4_gemm_plan: {"kernel": "tcgen05" | "narrow", "swap", "bn", "cta_group", "splits", "launches"}."""
+    info = PlanInfo()
+    cfg = ctypes.byref(config) if config is not None else None
+    _check(load().fp4_gemm_plan(FMT[fmt], int(bool(prepacked)), int(M), int(N), int(K), OUT[out], ACT[act], cfg,
+                                ctypes.byref(info)), "fp4_gemm_plan")
+    return {"kernel": "narrow" if info.kernel == 1 else "tcgen05", "swap": bool(info.swap), "bn": info.bn,
+            "cta_group": info.cta_group, "splits": info.splits, "launches": info.launches}
 
 
 def _named(name):

@@ -1,9 +1,9 @@
 """Builds the CUDA library (libfp4gemm.so) in-tree with nvcc for sm_103a.
 
-Two translation units (the GEMM and the quantiser) compiled in parallel, one
--gencode, then linked into one shared library; the static CUDA runtime is
-linked in and the driver's tensor-map encoder is looked up at run time, so the
-library needs no -lcuda.
+Three translation units (the tcgen05 GEMM, the narrow-M kernel and the
+quantiser) compiled in parallel, one -gencode, then linked into one shared
+library; the static CUDA runtime is linked in and the driver's tensor-map
+encoder is looked up at run time, so the library needs no -lcuda.
 """
 from __future__ import annotations
 
@@ -16,8 +16,9 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libfp4gemm.so")
-SOURCES = [os.path.join(CSRC, "fp4_gemm.cu"), os.path.join(CSRC, "fp4_quant.cu")]
-DEPS = SOURCES + [os.path.join(CSRC, "ptx.cuh"), os.path.join(INCLUDE, "fp4_gemm.h"),
+SOURCES = [os.path.join(CSRC, "fp4_gemm.cu"), os.path.join(CSRC, "fp4_quant.cu"), os.path.join(CSRC, "fp4_gemv.cu")]
+DEPS = SOURCES + [os.path.join(CSRC, "ptx.cuh"), os.path.join(CSRC, "epilogue.cuh"), os.path.join(CSRC, "fp4_gemv.cuh"),
+                  os.path.join(INCLUDE, "fp4_gemm.h"),
                   os.path.join(INCLUDE, "fp4_quant.h")]
 
 ARCH = "-gencode=arch=compute_103a,code=sm_103a"

@@ -52,7 +52,9 @@
 #include <cstring>
 #include <mutex>
 
+#include "epilogue.cuh"
 #include "fp4_gemm.h"
+#include "fp4_gemv.cuh"
 #include "ptx.cuh"
 
 namespace fp4 {
@@ -300,20 +302,6 @@ __device__ __forceinline__ void tmem_load_cols(uint32_t taddr, uint32_t *v)
             tmem_ld_32x32b_x32(taddr + 32 * c, r);
         }
     }
-}
-
-__device__ __forceinline__ float silu(float x) { return x / (1.0f + expf(-x)); }
-
-// The fused epilogue on one element: ReLU or squared ReLU (SwiGLU pairs two
-// elements and is done by the callers).
-__device__ __forceinline__ float activate(float z, int act)
-{
-    if (act == FP4_ACT_RELU) return fmaxf(z, 0.0f);
-    if (act == FP4_ACT_RELU2) {
-        const float r = fmaxf(z, 0.0f);
-        return r * r;
-    }
-    return z;
 }
 
 // One warp stores a 32-row x 32-byte chunk of D: lane l holds row row0 + l's
@@ -1021,6 +1009,23 @@ int pow2_bn(int64_t rows)
     return 256;
 }
 
+// The narrow-M CUDA-core kernel: forced by mode 3 (M <= kGemvMaxM), or chosen
+// automatically where it measured faster than the tcgen05 path on 28672 x 4096:
+// M <= 2 with plain scales (it needs no scale reorder), M == 1 with prepacked
+// ones. Either way only when its shared staging of A fits and B's scales are
+// 2-byte aligned (it reads NVFP4 scale pairs as 16-bit words).
+fp4_status choose_gemv(int64_t M, int64_t K, bool mx, int prepacked, const fp4_gemm_config *cfg, bool sfb_even,
+                       bool &gemv)
+{
+    const int mode = cfg ? cfg->mode : 0;
+    if (mode < 0 || mode > 3) return FP4_ERR_INVALID_ARG;
+    const bool fits = gemv_smem_bytes(M, K, mx) != 0;
+    if (mode == 3 && !fits) return FP4_ERR_UNSUPPORTED;
+    if (mode == 3 && !sfb_even) return FP4_ERR_MISALIGNED;
+    gemv = mode == 3 || (mode == 0 && fits && sfb_even && M <= (prepacked ? 1 : 2));
+    return FP4_OK;
+}
+
 // Chooses direct vs swap-AB, the tile N, the CTA group, the K split and the
 // k-tiles per stage. `rows_ok` says whether D's rows take 16-byte vector stores
 // (pitch a multiple of 16 bytes), which direct mode needs.
@@ -1028,7 +1033,7 @@ fp4_status make_plan(int64_t M, int64_t N, int64_t K, bool rows_ok, bool mx, int
                      Plan &p)
 {
     const int mode = cfg ? cfg->mode : 0;
-    if (mode < 0 || mode > 2) return FP4_ERR_INVALID_ARG;
+    if (mode < 0 || mode > 2) return FP4_ERR_INVALID_ARG;   // (mode 3 never reaches here)
     if (mode == 1)
         p.swap = false;
     else if (mode == 2)
@@ -1147,6 +1152,30 @@ fp4_status gemm_impl(fp4_format fmt, int prepacked, const void *A, const void *s
     const int vec = mx ? 32 : 16;
     const int64_t ksf = K / vec;
     const int64_t kc4 = cdiv(ksf, 4);
+    bool gemv = false;
+    if ((st = choose_gemv(M, K, mx, prepacked, cfg, (reinterpret_cast<uintptr_t>(sfB) & 1u) == 0, gemv)) != FP4_OK) return st;
+    if (gemv) {
+        // M <= 4: the CUDA-core kernel streams B once, reading the scales in
+        // either layout in place (no reorder, no scratch)
+        GemvParams g;
+        std::memset(&g, 0, sizeof g);
+        g.A = static_cast<const uint8_t *>(A);
+        g.sfA = static_cast<const uint8_t *>(sfA);
+        g.B = static_cast<const uint8_t *>(B);
+        g.sfB = static_cast<const uint8_t *>(sfB);
+        g.D = D;
+        g.ldd = d_cols;
+        g.M = static_cast<int32_t>(M);
+        g.N = static_cast<int32_t>(N);
+        g.K = static_cast<int32_t>(K);
+        g.mx = mx;
+        g.atoms = prepacked ? 1 : 0;
+        g.bf16 = out == FP4_OUT_BF16;
+        g.act = act;
+        g.alpha = alpha;
+        g.bias = bias;
+        return launch_gemv(g, info->sms, stream) == cudaSuccess ? FP4_OK : FP4_ERR_CUDA;
+    }
     const bool rows_ok = (d_cols * esize) % 16 == 0;
     Plan plan;
     st = make_plan(M, N, K, rows_ok, mx, info->sms, cfg, plan);
@@ -1302,6 +1331,42 @@ fp4_status fp4_gemm(fp4_format fmt, int scales_prepacked, const void *A, const v
                     const fp4_gemm_config *cfg, cudaStream_t stream)
 {
     return gemm_impl(fmt, scales_prepacked, A, sfA, B, sfB, alpha, D, M, N, K, out, cfg, stream);
+}
+
+fp4_status fp4_gemm_plan(fp4_format fmt, int scales_prepacked, int64_t M, int64_t N, int64_t K, fp4_out_dtype out,
+                         int32_t act, const fp4_gemm_config *cfg, fp4_plan_info *info)
+{
+    if (!info) return FP4_ERR_INVALID_ARG;
+    std::memset(info, 0, sizeof *info);
+    if (fmt != FP4_FMT_NVFP4 && fmt != FP4_FMT_MXFP4) return FP4_ERR_INVALID_ARG;
+    if (out != FP4_OUT_F32 && out != FP4_OUT_BF16) return FP4_ERR_INVALID_ARG;
+    if (act < FP4_ACT_NONE || act > FP4_ACT_SWIGLU) return FP4_ERR_INVALID_ARG;
+    if (M < 0 || N < 0 || K < 0) return FP4_ERR_INVALID_ARG;
+    if (act == FP4_ACT_SWIGLU && N % 2 != 0) return FP4_ERR_UNSUPPORTED;
+    if (K % 32 != 0) return FP4_ERR_UNSUPPORTED;
+    if (M == 0 || N == 0 || K == 0) return FP4_OK;      // no GEMM kernel (K == 0: a fill)
+    int dev;
+    DeviceInfo *di;
+    fp4_status st = device_info(dev, di);
+    if (st != FP4_OK) return st;
+    const bool mx = fmt == FP4_FMT_MXFP4;
+    bool gemv = false;
+    if ((st = choose_gemv(M, K, mx, scales_prepacked, cfg, true, gemv)) != FP4_OK) return st;
+    if (gemv) {
+        info->kernel = 1;
+        info->launches = 1;
+        return FP4_OK;
+    }
+    const int64_t esize = out == FP4_OUT_BF16 ? 2 : 4;
+    const int64_t d_cols = act == FP4_ACT_SWIGLU ? N / 2 : N;
+    Plan plan;
+    if ((st = make_plan(M, N, K, (d_cols * esize) % 16 == 0, mx, di->sms, cfg, plan)) != FP4_OK) return st;
+    info->swap = plan.swap;
+    info->bn = plan.bn;
+    info->cta_group = plan.cg;
+    info->splits = static_cast<int32_t>(cdiv(cdiv(K, kBK), cdiv(cdiv(K, kBK), plan.splits)));
+    info->launches = (scales_prepacked ? 0 : 2) + 1 + (info->splits > 1 ? 1 : 0);
+    return FP4_OK;
 }
 
 fp4_status fp4_gemm_fused(fp4_format fmt, int scales_prepacked, const void *A, const void *sfA, const void *B,

@@ -74,7 +74,15 @@ typedef enum { FP4_FMT_NVFP4 = 0, FP4_FMT_MXFP4 = 1 } fp4_format;
  *   mode:      0 auto; 1 direct (A on the MMA's M side, D written by TMA
  *              stores); 2 swap-AB (B on the M side, D^T tiles written with
  *              coalesced stores; the trick of "Hopper GEMM in CUTLASS C++ and
- *              the CuTe DSL, part 1", section on the swapped operands).
+ *              the CuTe DSL, part 1", section on the swapped operands);
+ *              3 the narrow-M CUDA-core kernel (M <= 4; it reads both scale
+ *              layouts in place, so it launches no reorder and needs no
+ *              scratch; sfB must be 2-byte aligned). Auto picks 3 for M <= 2
+ *              with plain scales and M == 1 with prepacked ones (where it
+ *              measured faster), when A's decoded rows fit its shared staging
+ *              (M * (K + K/vec * 4) bytes, K rounded up to 4096, at most
+ *              200 KB) and sfB is 2-byte aligned; else 2 for M <= 256, else 1.
+ *              The other fields apply to modes 1 and 2 only.
  *   bn:        0 auto; else the MMA N of a tile: 16, 32, 64, 128 or 256.
  *              Direct mode needs 128 or 256; so do several tiles on the N side.
  *   splits:    0 auto; else the number of K splits (swap-AB mode only).
@@ -88,6 +96,26 @@ typedef struct {
     int32_t max_ctas;
     int32_t cta_group;
 } fp4_gemm_config;
+
+/* What a call with these arguments would launch (no launch, nothing read):
+ *   kernel:    0 the tcgen05 GEMM, 1 the narrow-M CUDA-core kernel;
+ *   swap, bn, cta_group, splits: the tcgen05 plan (mode 1/2 semantics);
+ *   launches:  kernels one call launches (scale reorders, GEMM, split-K
+ *              reduce). Assumes 2-byte aligned scales. Needs an sm_103 device
+ *              (the plan depends on its SM count);
+ *   errors as the GEMM call's host validation. */
+typedef struct {
+    int32_t kernel;
+    int32_t swap;
+    int32_t bn;
+    int32_t cta_group;
+    int32_t splits;
+    int32_t launches;
+} fp4_plan_info;
+
+fp4_status fp4_gemm_plan(fp4_format fmt, int scales_prepacked, int64_t M, int64_t N, int64_t K,
+                         fp4_out_dtype out, int32_t act, const fp4_gemm_config *cfg,
+                         fp4_plan_info *info);
 
 /* NVFP4 GEMM (E4M3 scales, one per 16 K-elements), plain row-major scales. */
 fp4_status fp4_gemm_nvfp4(const void *A, const void *sfA, const void *B, const void *sfB,

@@ -116,6 +116,25 @@ def test_fused_host_validation_without_device(fp4):
     assert f(2, p, 64, 64, K=48) == 2              # K % 32 != 0
 
 
+def test_plan_host_validation_without_device(fp4):
+    lib = fp4.load()
+    info = fp4.PlanInfo()
+
+    def plan(fmt=0, M=1, N=64, K=64, out=0, act=0, cfg=None, ptr=True):
+        return lib.fp4_gemm_plan(fmt, 0, M, N, K, out, act, cfg, ctypes.byref(info) if ptr else None)
+
+    assert plan(ptr=False) == 1
+    assert plan(fmt=3) == 1
+    assert plan(out=2) == 1
+    assert plan(act=5) == 1
+    assert plan(M=-1) == 1
+    assert plan(K=40) == 2
+    assert plan(N=63, act=3) == 2
+    info.launches = 7
+    assert plan(M=0) == 0 and info.launches == 0          # nothing to launch
+    assert plan(cfg=ctypes.byref(fp4.GemmConfig(mode=4))) in (1, 6)   # bad mode (or no device first)
+
+
 def test_quantize_host_validation_without_device(fp4):
     buf = np.zeros(4096 + 16, np.uint8)
     p = buf.ctypes.data + (-buf.ctypes.data) % 16
