@@ -16,6 +16,9 @@ Functions (each follows the passage cited in ``oracle.c``):
   (interleaved gate, up columns) on fp64 GEMM results.
 * ``quantize(X, fmt)`` -> (packed E2M1 codes, plain row-major scale bytes) of
   fp32 or bf16 values, one scale per 16 (nvfp4) or 32 (mxfp4) values.
+* ``grouped_gemm_rows(gin, rows=None)`` -> (D64, absdot): the grouped (MoE)
+  GEMM -- independent GEMMs on consecutive row ranges of A and D, group g
+  with its own weight matrix B_g.
 
 Parity status of each function is recorded in the module docstrings of
 ``tests/test_oracle.py``; every function here is pinned there.
@@ -223,3 +226,47 @@ def epilogue(y: np.ndarray, bias, op: str) -> np.ndarray:
     if rc != 0:
         raise ValueError("oracle_epilogue rejected its arguments")
     return out
+
+
+# ---- grouped GEMM (mixture-of-experts layers) --------------------------------
+#
+# A grouped GEMM is a set of independent GEMMs sharing N and K: group g owns
+# rows offsets[g] .. offsets[g+1]-1 of A (and of D) and the weight matrix B_g,
+# rows g*N .. g*N+N-1 of the stacked B (the NVFP4 ReLU-squared MoE workload of
+# "TMA Pipelines, Tensor Cores, and ctm-rs Interop", "Where to Go Next": each
+# expert applies its own weights to the tokens routed to it). Each group's
+# rows are computed by gemm_rows on that group's slices -- nothing else.
+
+class _GroupProblem:
+    """One group's GEMM as gemm_rows takes it."""
+
+    def __init__(self, gin, g):
+        o0, o1 = int(gin.offsets[g]), int(gin.offsets[g + 1])
+        K, vec, N = int(gin.K), int(gin.vec), int(gin.N)
+        self.A = gin.A.reshape(-1, K // 2)[o0:o1]
+        self.sfA = gin.sfA.reshape(-1, K // vec)[o0:o1]
+        self.B = gin.B.reshape(-1, K // 2)[g * N:(g + 1) * N]
+        self.sfB = gin.sfB.reshape(-1, K // vec)[g * N:(g + 1) * N]
+        self.M, self.N, self.K, self.vec, self.alpha = o1 - o0, N, K, vec, gin.alpha
+
+
+def _group_of_rows(offsets: np.ndarray, rows: np.ndarray) -> np.ndarray:
+    """Group of each D row: the g with offsets[g] <= row < offsets[g+1]."""
+    return np.searchsorted(offsets, rows, side="right") - 1
+
+
+def grouped_gemm_rows(gin, rows=None, nthreads: int = 0):
+    """D rows (fp64, before output rounding) and |alpha|*sum|a b| of a grouped
+    GEMM. gin: fmt, offsets (G+1, int64), N, K, vec, alpha, A [M_total][K/2],
+    sfA [M_total][K/vec], B [G*N][K/2], sfB [G*N][K/vec]."""
+    offsets = np.asarray(gin.offsets, dtype=np.int64)
+    m_total = int(offsets[-1])
+    rows = np.arange(m_total, dtype=np.int64) if rows is None else np.asarray(rows, dtype=np.int64)
+    D = np.empty((rows.size, int(gin.N)), dtype=np.float64)
+    absd = np.empty_like(D)
+    groups = _group_of_rows(offsets, rows)
+    for g in np.unique(groups):
+        sel = np.nonzero(groups == g)[0]
+        d, a = gemm_rows(_GroupProblem(gin, int(g)), rows[sel] - offsets[g], nthreads=nthreads)
+        D[sel], absd[sel] = d, a
+    return D, absd

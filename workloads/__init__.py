@@ -262,6 +262,89 @@ def make_fused(name: str, seed: int = 0):
     return inp, w["act"], bias
 
 
+# ---- grouped (mixture-of-experts) GEMMs -----------------------------------------
+#
+# A grouped GEMM is one GEMM per expert: expert g applies its weights B_g
+# (N x K) to the rows routed to it, which sit at rows offsets[g] ..
+# offsets[g+1]-1 of A and D. The routed workloads below draw, for T tokens,
+# `top` distinct experts per token with probability proportional to
+# (rank + 1)^-0.8 over a seeded random ranking of the experts (a skewed load,
+# some experts empty at small T), and sort the routed rows by expert.
+
+
+@dataclasses.dataclass
+class GroupedInputs:
+    fmt: str
+    offsets: np.ndarray      # int64 [G + 1]: group g = rows offsets[g] .. offsets[g+1]-1
+    N: int
+    K: int
+    A: np.ndarray            # uint8 [M_total][K/2]
+    sfA: np.ndarray          # uint8 [M_total][K/vec]
+    B: np.ndarray            # uint8 [G*N][K/2]: B_g = rows g*N .. g*N+N-1
+    sfB: np.ndarray          # uint8 [G*N][K/vec]
+    alpha: float
+    out: str
+    name: str = ""
+
+    @property
+    def G(self) -> int:
+        return len(self.offsets) - 1
+
+    @property
+    def M(self) -> int:
+        return int(self.offsets[-1])
+
+    @property
+    def vec(self) -> int:
+        return NV_VEC if self.fmt == "nvfp4" else MX_VEC
+
+    @property
+    def flops(self) -> float:
+        return 2.0 * self.M * self.N * self.K
+
+
+def make_grouped(fmt: str, sizes, N: int, K: int, *, a_std: float = 1.0, b_std: float = 1.0, alpha: float = 1.0,
+                 out: str = "f32", seed: int = 0, name: str = "") -> GroupedInputs:
+    """Group g has sizes[g] rows; values N(0, a_std^2) / N(0, b_std^2), quantised blockwise."""
+    sizes = np.asarray(sizes, dtype=np.int64)
+    offsets = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int64)
+    ra = np.random.default_rng(2 * seed)
+    rb = np.random.default_rng(2 * seed + 1)
+    A, sfA = _quantize_rows(_normal(ra, a_std), int(offsets[-1]), K, fmt)
+    B, sfB = _quantize_rows(_normal(rb, b_std), len(sizes) * N, K, fmt)
+    return GroupedInputs(fmt, offsets, N, K, A, sfA, B, sfB, float(alpha), out, name)
+
+
+def route_tokens(tokens: int, experts: int, top: int, seed: int = 0) -> np.ndarray:
+    """Rows per expert after routing `tokens` tokens to `top` distinct experts each."""
+    rng = np.random.default_rng(500 + seed)
+    rank = rng.permutation(experts)
+    p = (rank + 1.0) ** -0.8
+    p /= p.sum()
+    counts = np.zeros(experts, dtype=np.int64)
+    for _ in range(tokens):
+        counts[rng.choice(experts, size=top, replace=False, p=p)] += 1
+    return counts
+
+
+GROUPED_WORKLOADS = {
+    # an expert up-projection of a squared-ReLU MoE: 64 experts, d_model 4096,
+    # expert width 2048, top-8 routing; prefill (4096 tokens) and decode (64)
+    "moe_nvfp4_e64_t4096_top8_n2048_k4096": dict(fmt="nvfp4", experts=64, tokens=4096, top=8, N=2048, K=4096,
+                                                 out="bf16", act="relu2"),
+    "moe_nvfp4_e64_t64_top8_n2048_k4096": dict(fmt="nvfp4", experts=64, tokens=64, top=8, N=2048, K=4096,
+                                               out="bf16", act="relu2"),
+}
+
+
+def make_grouped_workload(name: str, seed: int = 0):
+    """(GroupedInputs, act) of a named MoE workload."""
+    w = GROUPED_WORKLOADS[name]
+    sizes = route_tokens(w["tokens"], w["experts"], w["top"], seed)
+    gin = make_grouped(w["fmt"], sizes, w["N"], w["K"], a_std=1.0, b_std=0.02, out=w["out"], seed=seed, name=name)
+    return gin, w["act"]
+
+
 # ---- raw values for the quantisation step -------------------------------------
 #
 # The quantiser's inputs are plain activations: seeded draws rounded to the
