@@ -31,6 +31,13 @@ the FFN workloads ffn_*; same metric, roofline and legs, with the oracle's
 GEMM plus its epilogue as the cpu_baseline and e2e through pinned host
 buffers copied on the stream around the same call.
 
+--op grouped times the grouped (mixture-of-experts) GEMM, fp4_gemm_grouped,
+on the moe_* workloads: a step is the grouped reorder of the routed
+activations' scales, the reorder of the experts' weight scales and the one
+grouped GEMM launch over all experts (timed alone for the roofline; its
+events also cover the few-KB copy of the per-group tables). Same metric
+(2 * M_total * N * K per step).
+
 --op quantize measures the quantisation step that feeds the GEMM instead
 (fp4_quantize: bf16 or fp32 activations -> E2M1 codes + atom-layout scales),
 against the HBM roofline: its bytes (values read, codes and scale atoms
@@ -59,6 +66,7 @@ import workloads as W  # noqa: E402
 METRIC = "block-scaled FP4 GEMM TFLOP/s on 1 GB300 and % of dense FP4 tensor peak"
 DEFAULT_WORKLOAD = "nvfp4_4096_bf16"
 DEFAULT_FUSED_WORKLOAD = "ffn_swiglu_nvfp4_m8192_n28672_k4096"
+DEFAULT_GROUPED_WORKLOAD = "moe_nvfp4_e64_t4096_top8_n2048_k4096"
 FP4_PER_BF16 = 13.5 / 2.25       # nominal dense FP4 : dense bf16 tensor throughput on GB300
 FALLBACK_BF16_TFLOPS = 1900.0
 FALLBACK_HBM_GBS = 6800.0
@@ -527,15 +535,158 @@ def run_quant(args, rank, ws, local):
     return res
 
 
+def run_grouped(args, rank, ws, local):
+    """Times fp4_gemm_grouped on a named MoE workload."""
+    import torch
+    import block_scaled_fp4_sfa_gb300 as fp4
+    gin, act = W.make_grouped_workload(args.workload, seed=rank)
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    fp4.load()
+    stream = torch.cuda.current_stream()
+    s = stream.cuda_stream
+    vec, M, N, K, G = gin.vec, gin.M, gin.N, gin.K, gin.G
+    hA, hsA, hB, hsB = (torch.from_numpy(np.ascontiguousarray(getattr(gin, k))) for k in ("A", "sfA", "B", "sfB"))
+    A, sfA, B, sfB = (t.to(dev) for t in (hA, hsA, hB, hsB))
+    atomA = torch.empty(max(16, fp4.scale_atom_bytes_grouped(gin.offsets, K, vec)), dtype=torch.uint8, device=dev)
+    assert N % 128 == 0            # then one reorder of all G*N weight rows is the per-expert atom layout
+    atomB = torch.empty(fp4.scale_atom_bytes(G * N, K, vec), dtype=torch.uint8, device=dev)
+    odt = torch.float32 if gin.out == "f32" else torch.bfloat16
+    d_cols = N // 2 if act == "swiglu" else N
+    D = torch.empty(M, d_cols, dtype=odt, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def step():
+        fp4.scale_reorder_grouped(sfA, atomA, gin.offsets, K, vec, stream=s)
+        fp4.scale_reorder(sfB, atomB, G * N, K, vec, stream=s)
+        ev_g0.record(stream)
+        fp4.gemm_grouped(gin.fmt, gin.offsets, A, atomA, B, atomB, gin.alpha, D, N, K, gin.out, act=act,
+                         weights_prepacked=True, acts_prepacked=True, stream=s)
+        ev_g1.record(stream)
+
+    ev_g0 = torch.cuda.Event(enable_timing=True)
+    ev_g1 = torch.cuda.Event(enable_timing=True)
+    for _ in range(args.warmup):
+        flush.zero_()
+        torch.cuda._sleep(SPACER_CYCLES)
+        step()
+    torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    g0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    g1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local if not args.quick else -1) as clk:
+        time.sleep(0.2)
+        for i in range(args.steps):
+            flush.zero_()
+            torch.cuda._sleep(SPACER_CYCLES)
+            starts[i].record(stream)
+            ev_g0, ev_g1 = g0[i], g1[i]
+            step()
+            ends[i].record(stream)
+        torch.cuda.synchronize()
+        if ws > 1:
+            torch.distributed.barrier()
+    st = fp4.get_device_status(s)
+    if st != 0:
+        raise RuntimeError("device status after timing: %s" % fp4.status_string(st))
+    step_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+    gemm_ms = [a.elapsed_time(b) for a, b in zip(g0, g1)]
+    total_ms = slowest_rank_ms(sum(step_ms), ws, dev)
+    value = whole_job_tflops(gin.flops, args.steps, ws, total_ms)
+    sizes = np.diff(gin.offsets)
+    cfg = {"workload": gin.name, "format": gin.fmt, "experts": G, "M_total": M, "N": N, "K": K, "out": gin.out,
+           "epilogue": act, "rows_per_expert": {"min": int(sizes.min()), "max": int(sizes.max()),
+                                                "empty": int((sizes == 0).sum())},
+           "l2": "flushed between steps (256 MiB write, outside the step events)",
+           "parallelism": "replicas" if ws > 1 else "single"}
+    res = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
+           "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": "e2m1", "data": "synthetic", "config": cfg,
+           "gemm_us": 1e3 * sum(gemm_ms) / len(gemm_ms)}
+    if args.quick:
+        return res
+    # e2e: pinned host buffers copied in, the plain-scale grouped call, D copied back
+    pA, psA, pB, psB = (t.pin_memory() for t in (hA, hsA, hB, hsB))
+    pD = torch.empty(M, d_cols, dtype=odt).pin_memory()
+
+    def e2e_step():
+        for dst, src in ((A, pA), (sfA, psA), (B, pB), (sfB, psB)):
+            dst.copy_(src, non_blocking=True)
+        fp4.gemm_grouped(gin.fmt, gin.offsets, A, sfA, B, sfB, gin.alpha, D, N, K, gin.out, act=act, stream=s)
+        pD.copy_(D, non_blocking=True)
+
+    e_steps = max(3, min(args.steps, 20))
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e_steps
+    bf16_peak, hbm_peak, peak_src = peaks()
+    gemm_avg_ms = sum(gemm_ms) / len(gemm_ms)
+    achieved = gin.flops / (gemm_avg_ms * 1e-3) / 1e12
+    fp4_peak = bf16_peak * FP4_PER_BF16
+    used = int((sizes > 0).sum())
+    alg_bytes = (M * (K // 2 + K // vec) + used * N * (K // 2 + K // vec)
+                 + M * d_cols * (4 if gin.out == "f32" else 2))
+    achieved_gbs = alg_bytes / (gemm_avg_ms * 1e-3) / 1e9
+    if gin.flops / alg_bytes < fp4_peak * 1e12 / (hbm_peak * 1e9):
+        roofline = {"bound": "hbm", "achieved": achieved_gbs, "peak": hbm_peak, "unit": "GB/s",
+                    "frac": achieved_gbs / hbm_peak, "peak_source": "%s HBM copy bandwidth" % peak_src,
+                    "tensor_tflops": achieved, "tensor_frac": achieved / fp4_peak}
+    else:
+        roofline = {"bound": "tensor", "achieved": achieved, "peak": fp4_peak, "unit": "TFLOP/s",
+                    "frac": achieved / fp4_peak, "peak_source": "%s bf16 burst %.1f TFLOP/s x %.0f (nominal FP4:bf16)"
+                    % (peak_src, bf16_peak, FP4_PER_BF16)}
+    roofline.update({"traffic": ncu_traffic(gin.name), "kernel": "fp4_gemm_kernel (grouped)",
+                     "gemm_us": 1e3 * gemm_avg_ms, "algorithmic_bytes": alg_bytes,
+                     "hbm_frac_at_algorithmic_bytes": achieved_gbs / hbm_peak})
+    res.update({
+        "roofline": roofline,
+        "e2e": {"value": gin.flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in (hA, hsA, hB, hsB)),
+                "d2h_bytes_per_step": pD.numel() * pD.element_size()},
+        "gpu_launches": 3 * args.steps,
+        "clocks": clk.summary(),
+    })
+    if rank == 0 and not args.no_cpu_baseline:
+        import oracle
+        probe = np.arange(min(8, M))
+        oracle.grouped_gemm_rows(gin, probe[:1])
+        t0 = time.perf_counter()
+        oracle.grouped_gemm_rows(gin, probe)
+        per_row = (time.perf_counter() - t0) / len(probe)
+        n = int(max(1, min(M, args.cpu_sample_s / max(per_row, 1e-9))))
+        rows = np.linspace(0, M - 1, n).astype(np.int64)
+        t0 = time.perf_counter()
+        y, _ = oracle.grouped_gemm_rows(gin, rows)
+        oracle.epilogue(y, None, act)
+        dt = time.perf_counter() - t0
+        res["cpu_baseline"] = {"value": 2.0 * n * N * K / dt / 1e12, "unit": "TFLOP/s", "cores": os.cpu_count(),
+                               "kind": "oracle",
+                               "sample": "%d of %d routed rows of %s (all %d columns), %.1f s, fp64 C oracle per "
+                                         "expert + its %s epilogue" % (n, M, gin.name, N, dt, act)}
+    return res
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--op", choices=["gemm", "fused", "quantize"], default="gemm")
+    ap.add_argument("--op", choices=["gemm", "fused", "grouped", "quantize"], default="gemm")
     ap.add_argument("--workload", default=None,
-                    choices=W.config_names() + sorted(W.FUSED_WORKLOADS) + sorted(W.QUANT_WORKLOADS))
+                    choices=W.config_names() + sorted(W.FUSED_WORKLOADS) + sorted(W.GROUPED_WORKLOADS)
+                    + sorted(W.QUANT_WORKLOADS))
     ap.add_argument("--cpu-sample-s", type=float, default=12.0, help="oracle seconds for cpu_baseline")
     ap.add_argument("--ref-step-s", type=float, default=3.0, help="oracle seconds per reference step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -547,21 +698,21 @@ def main():
         ap.error("--warmup must be >= 3")
     ws, rank, local = dist_env()
     if args.workload is None:
-        args.workload = {"quantize": DEFAULT_QUANT_WORKLOAD, "fused": DEFAULT_FUSED_WORKLOAD}.get(
-            args.op, DEFAULT_WORKLOAD)
-    table = {"quantize": W.QUANT_WORKLOADS, "fused": W.FUSED_WORKLOADS}.get(args.op)
+        args.workload = {"quantize": DEFAULT_QUANT_WORKLOAD, "fused": DEFAULT_FUSED_WORKLOAD,
+                         "grouped": DEFAULT_GROUPED_WORKLOAD}.get(args.op, DEFAULT_WORKLOAD)
+    table = {"quantize": W.QUANT_WORKLOADS, "fused": W.FUSED_WORKLOADS, "grouped": W.GROUPED_WORKLOADS}.get(args.op)
     valid = table if table is not None else W.config_names()
     if args.workload not in valid:
         ap.error("--op %s does not take workload %s" % (args.op, args.workload))
     if args.op != "gemm" and args.impl == "reference":
         ap.error("--impl reference times the GEMM's oracle; use --op gemm")
 
-    if args.op == "quantize":
+    if args.op in ("quantize", "grouped"):
         if ws > 1:
             import torch
             torch.cuda.set_device(local)
             torch.distributed.init_process_group("nccl")
-        res = run_quant(args, rank, ws, local)
+        res = (run_quant if args.op == "quantize" else run_grouped)(args, rank, ws, local)
         if ws > 1:
             import torch
             torch.distributed.destroy_process_group()

@@ -20,7 +20,8 @@ from . import _build
 __all__ = ["FP4_OK", "Fp4Error", "load", "build", "gemm", "gemm_nvfp4", "gemm_mxfp4", "gemm_nvfp4_prepacked",
            "gemm_mxfp4_prepacked", "gemm_host", "scale_reorder", "scale_atom_bytes", "get_device_status",
            "status_string", "set_wait_limit_ms", "GemmConfig", "FMT", "OUT", "gemm_static_scratch",
-           "STATIC_SCRATCH_BYTES", "quantize", "IN", "SF_LAYOUT", "gemm_fused", "ACT", "Epilogue", "gemm_plan", "PlanInfo"]
+           "STATIC_SCRATCH_BYTES", "quantize", "IN", "SF_LAYOUT", "gemm_fused", "ACT", "Epilogue", "gemm_plan", "PlanInfo", "gemm_grouped", "scale_reorder_grouped",
+           "scale_atom_bytes_grouped"]
 
 FP4_OK = 0
 STATUS_NAMES = {0: "FP4_OK", 1: "FP4_ERR_INVALID_ARG", 2: "FP4_ERR_UNSUPPORTED", 3: "FP4_ERR_MISALIGNED",
@@ -82,6 +83,13 @@ def load():
     lib.fp4_gemm_fused.argtypes = [i32, i32, vp, vp, vp, vp, f32, ctypes.POINTER(Epilogue), vp, i64, i64, i64, i32,
                                    ctypes.POINTER(GemmConfig), vp]
     lib.fp4_gemm_fused.restype = i32
+    lib.fp4_gemm_grouped.argtypes = [i32, i32, i64, vp, vp, vp, vp, vp, f32, ctypes.POINTER(Epilogue), vp, i64, i64,
+                                     i32, ctypes.POINTER(GemmConfig), vp]
+    lib.fp4_gemm_grouped.restype = i32
+    lib.fp4_scale_atom_bytes_grouped.argtypes = [i64, vp, i64, i32]
+    lib.fp4_scale_atom_bytes_grouped.restype = ctypes.c_size_t
+    lib.fp4_scale_reorder_grouped.argtypes = [vp, vp, i64, vp, i64, i32, vp]
+    lib.fp4_scale_reorder_grouped.restype = i32
     lib.fp4_gemm_plan.argtypes = [i32, i32, i64, i64, i64, i32, i32, ctypes.POINTER(GemmConfig),
                                   ctypes.POINTER(PlanInfo)]
     lib.fp4_gemm_plan.restype = i32
@@ -157,6 +165,43 @@ def gemm_fused(fmt: str, A, sfA, B, sfB, alpha: float, D, M: int, N: int, K: int
                                ctypes.byref(epi), _ptr(D), int(M), int(N), int(K), OUT[out], cfg, _stream(stream))
     if check:
         _check(st, "fp4_gemm_fused")
+    return st
+
+
+def _offsets(offsets):
+    import numpy as np
+    return np.ascontiguousarray(np.asarray(offsets, dtype=np.int64))
+
+
+def scale_atom_bytes_grouped(offsets, K: int, vec: int) -> int:
+    offs = _offsets(offsets)
+    return int(load().fp4_scale_atom_bytes_grouped(int(offs.size - 1), offs.ctypes.data, int(K), int(vec)))
+
+
+def scale_reorder_grouped(sf, out, offsets, K: int, vec: int, stream=None, check: bool = True) -> int:
+    """fp4_scale_reorder_grouped: activation scales -> the grouped atom layout."""
+    offs = _offsets(offsets)
+    st = load().fp4_scale_reorder_grouped(_ptr(sf), _ptr(out), int(offs.size - 1), offs.ctypes.data, int(K),
+                                          int(vec), _stream(stream))
+    if check:
+        _check(st, "fp4_scale_reorder_grouped")
+    return st
+
+
+def gemm_grouped(fmt: str, offsets, A, sfA, B, sfB, alpha: float, D, N: int, K: int, out: str = "f32", *,
+                 act: str = "none", bias=None, weights_prepacked: bool = False, acts_prepacked: bool = False,
+                 config: GemmConfig | None = None, stream=None, check: bool = True) -> int:
+    """fp4_gemm_grouped: group g = rows offsets[g] .. offsets[g+1]-1 of A and D, weights B[g]. ``offsets``
+    is a host sequence of G + 1 integers; bias, if given, is [G][N] on the device."""
+    offs = _offsets(offsets)
+    epi = Epilogue(ACT[act], _ptr(bias))
+    cfg = ctypes.byref(config) if config is not None else None
+    flags = (1 if weights_prepacked else 0) | (2 if acts_prepacked else 0)
+    st = load().fp4_gemm_grouped(FMT[fmt], flags, int(offs.size - 1), offs.ctypes.data,
+                                 _ptr(A), _ptr(sfA), _ptr(B), _ptr(sfB), float(alpha), ctypes.byref(epi), _ptr(D),
+                                 int(N), int(K), OUT[out], cfg, _stream(stream))
+    if check:
+        _check(st, "fp4_gemm_grouped")
     return st
 
 

@@ -51,6 +51,7 @@
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
+#include <vector>
 
 #include "epilogue.cuh"
 #include "fp4_gemm.h"
@@ -80,6 +81,27 @@ constexpr int kSmemLimit = 232448;
 
 enum EpiMode : int32_t { kEpiRows = 0, kEpiTransposed = 1, kEpiSplitK = 2 };
 
+// Grouped GEMM (fp4_gemm_grouped): where one group's tiles sit in the operands.
+// Unit u of group g is tile (ta, tb) with u - first = tb * tiles_a + ta. Slot
+// A's local row r is TMA row oa + r, scale block sa + r / 128 and D index
+// da + r; rows r >= la are outside the group. Slot B likewise.
+struct GroupGeo {
+    int32_t first, tiles_a;
+    int32_t oa, sa, da, la;
+    int32_t ob, sb, db, lb;
+    int32_t bias_off;        // first bias entry of the group
+    int32_t pad;
+};
+static_assert(sizeof(GroupGeo) == 48, "three 16-byte loads");
+
+// A unit's tile and where it sits (the whole problem when not grouped).
+struct TileGeo {
+    int ta, tb;
+    int oa, sa, da, la;
+    int ob, sb, db, lb;
+    int bias_off;
+};
+
 struct Args {
     void *out;               // D (modes 0, 1) or split-K workspace (mode 2)
     int64_t ldo;             // row stride in elements of `out`
@@ -101,8 +123,17 @@ struct Args {
     // the second half adds it.
     int32_t split_units;
     int32_t kh;                          // k-tiles of a first half
-    float *tail_ws;                      // [tail tile][CTA of the pair][BN][128]
-    unsigned long long *tail_flags;      // [tail tile][CTA of the pair]
+    union {                              // (the parameter block keeps its size: a larger one
+                                         // costs the widest variants a register spill)
+        struct {                         // split tail
+            float *tail_ws;              // [tail tile][CTA of the pair][BN][128]
+            unsigned long long *tail_flags;   // [tail tile][CTA of the pair]
+        };
+        struct {                         // grouped kernels: unit -> group, each group's geometry
+            const int32_t *unit_group;
+            const GroupGeo *geo;
+        };
+    };
     unsigned long long epoch;            // this launch's flag value
 };
 
@@ -263,12 +294,53 @@ __device__ __forceinline__ void unit_coords(const Args &a, int u, int &ta, int &
     ta = r / gw;
 }
 
+// Where unit u's tile sits; ta / tb as unit_work gives them when not grouped.
+template <bool GROUPED>
+__device__ __forceinline__ void tile_geo(const Args &a, int u, int ta, int tb, TileGeo &t)
+{
+    if constexpr (GROUPED) {
+        const int g = __ldg(a.unit_group + u);
+        const int4 *p = reinterpret_cast<const int4 *>(a.geo + g);
+        const int4 w0 = __ldg(p), w1 = __ldg(p + 1), w2 = __ldg(p + 2);
+        const int lu = u - w0.x;
+        t.tb = lu / w0.y;
+        t.ta = lu - t.tb * w0.y;
+        t.oa = w0.z;
+        t.sa = w0.w;
+        t.da = w1.x;
+        t.la = w1.y;
+        t.ob = w1.z;
+        t.sb = w1.w;
+        t.db = w2.x;
+        t.lb = w2.y;
+        t.bias_off = w2.z;
+        return;
+    }
+    else {
+        t.ta = ta;
+        t.tb = tb;
+        t.oa = t.sa = t.da = 0;
+        t.la = a.rows_a;
+        t.ob = t.sb = t.db = 0;
+        t.lb = a.rows_b;
+        t.bias_off = 0;
+    }
+}
+
 // Unit u -> its tile and k-tile range. half = -1 for a whole tile (or a
 // split-K unit); 0 / 1 for the first / second K half of a split tile, whose
 // index among the split tiles is tidx.
+template <bool GROUPED>
 __device__ __forceinline__ void unit_work(const Args &a, int u, int &ta, int &tb, int &split, int &kt0, int &kt1,
                                           int &half, int &tidx)
 {
+    if constexpr (GROUPED) {          // whole tiles (tile_geo gives ta, tb)
+        ta = tb = split = tidx = 0;
+        kt0 = 0;
+        kt1 = a.k_tiles;
+        half = -1;
+        return;
+    }
     if (u >= a.split_units) {
         unit_coords(a, u - a.split_units / 2, ta, tb, split);
         kt0 = split * a.kps;
@@ -329,7 +401,7 @@ __device__ __forceinline__ void store_chunk32(uint8_t *stg, const uint32_t (&w)[
     __syncwarp();
 }
 
-template <int CG, int BN, bool MX>
+template <int CG, int BN, bool MX, bool GROUPED>
 __global__ void __launch_bounds__(kThreads, 1)
     fp4_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                     const __grid_constant__ CUtensorMap tmap_sfa, const __grid_constant__ CUtensorMap tmap_sfb,
@@ -399,11 +471,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = true;
             for (int u = pair; ok && u < args.units; u += npairs) {
                 int ta, tb, split, kt0, kt1, half, tidx;
-                unit_work(args, u, ta, tb, split, kt0, kt1, half, tidx);
-                const int rba = ta * CG + static_cast<int>(rank);       // this CTA's 128-row block of slot A
-                const int row_a = rba * kBM;
-                const int row_b = tb * BN + static_cast<int>(rank) * C::BN_CTA;
-                const int rbb = (tb * BN) / 128;                         // first scale block of the N side
+                unit_work<GROUPED>(args, u, ta, tb, split, kt0, kt1, half, tidx);
+                TileGeo tg;
+                tile_geo<GROUPED>(args, u, ta, tb, tg);
+                const int rba = tg.ta * CG + static_cast<int>(rank);     // this CTA's 128-row block of slot A
+                const int row_a = tg.oa + rba * kBM;
+                const int row_b = tg.ob + tg.tb * BN + static_cast<int>(rank) * C::BN_CTA;
+                const int sba = tg.sa + rba;                             // its scale block
+                const int rbb = tg.sb + (tg.tb * BN) / 128;              // first scale block of the N side
                 for (int kt = kt0; kt < kt1; ++kt) {
                     if (!wait(bar_empty + 8 * stage, phase ^ 1u, args.wait_ns, abort_flag)) {
                         ok = false;
@@ -415,7 +490,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tma_load_2d<CG>(base + C::OFF_A + slot * C::A_BYTES, &tmap_a, full, kt * kBKBytes, row_a);
                     tma_load_2d<CG>(base + C::OFF_B + slot * C::B_BYTES, &tmap_b, full, kt * kBKBytes, row_b);
                     tma_load_2d<CG>(base + C::OFF_SFA + slot * C::SFA_BYTES, &tmap_sfa, full,
-                                    kt * C::APK * (kAtomBytes / 8), rba);
+                                    kt * C::APK * (kAtomBytes / 8), sba);
                     tma_load_2d<CG>(base + C::OFF_SFB + slot * C::SFB_BYTES, &tmap_sfb, full,
                                     kt * C::APK * (kAtomBytes / 8), rbb);
                     filled |= 1u << stage;
@@ -453,7 +528,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = true;
             for (int u = pair; ok && u < args.units; u += npairs) {
                 int ta, tb, split, kt0, kt1, half, tidx;
-                unit_work(args, u, ta, tb, split, kt0, kt1, half, tidx);
+                unit_work<GROUPED>(args, u, ta, tb, split, kt0, kt1, half, tidx);
                 // the epilogue has drained this accumulator (once per tile)
                 if (!wait_cluster(bar_acc_empty + 8 * acc, acc_phase ^ 1u, args.wait_ns, abort_flag)) break;
                 const uint32_t d_tmem = tmem + static_cast<uint32_t>(acc * BN);
@@ -520,7 +595,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = true;
             for (int u = pair; ok && u < args.units; u += npairs) {
                 int ta, tb, split, kt0, kt1, half, tidx;
-                unit_work(args, u, ta, tb, split, kt0, kt1, half, tidx);
+                unit_work<GROUPED>(args, u, ta, tb, split, kt0, kt1, half, tidx);
                 for (int kt = kt0; kt < kt1; ++kt) {
                     if (!wait(bar_full + 8 * stage, phase, args.wait_ns, abort_flag)) {
                         ok = false;
@@ -547,7 +622,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t acc_phase = 0;
         for (int u = pair; u < args.units; u += npairs) {
             int ta, tb, split, kt0, kt1, half, tidx;
-            unit_work(args, u, ta, tb, split, kt0, kt1, half, tidx);
+            unit_work<GROUPED>(args, u, ta, tb, split, kt0, kt1, half, tidx);
+            TileGeo tg;
+            tile_geo<GROUPED>(args, u, ta, tb, tg);
             if (!wait(bar_acc_full + 8 * acc, acc_phase, args.wait_ns, abort_flag)) break;
             tc_fence_after();
             // Drain this warp's 32 lanes x BN/2 columns, then release the accumulator.
@@ -591,23 +668,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             if (store_d) {
-                const int row_base = (ta * CG + static_cast<int>(rank)) * kBM + 32 * q;   // this warp's first row
-                const int ra = row_base + lane;                                            // slot-A row of this lane
-                const int col0 = tb * BN + h * C::COLS_WARP;                                // first slot-B row
+                // local rows of the tile's problem (the group's, when grouped)
+                const int row_base = (tg.ta * CG + static_cast<int>(rank)) * kBM + 32 * q;  // this warp's first row
+                const int ra = row_base + lane;                                               // slot-A row of this lane
+                const int col0 = tg.tb * BN + h * C::COLS_WARP;                                // first slot-B row
                 const bool glu = args.act == FP4_ACT_SWIGLU;
                 if (args.mode != kEpiSplitK) {
                     // z = alpha * acc + bias, then the activation. Rows mode: v[i] is
                     // GEMM column col0 + i; transposed: every v[i] of this lane is
                     // GEMM column ra.
                     if (args.bias) {
+                        const float *bias = args.bias + tg.bias_off;
                         if (args.mode == kEpiRows) {
 #pragma unroll
                             for (int i = 0; i < C::COLS_WARP; ++i) {
-                                const float b = col0 + i < args.rows_b ? __ldg(args.bias + col0 + i) : 0.0f;
+                                const float b = col0 + i < tg.lb ? __ldg(bias + col0 + i) : 0.0f;
                                 v[i] = __float_as_uint(fmaf(__uint_as_float(v[i]), args.alpha, b));
                             }
                         } else {
-                            const float b = ra < args.rows_a ? __ldg(args.bias + ra) : 0.0f;
+                            const float b = ra < tg.la ? __ldg(bias + ra) : 0.0f;
 #pragma unroll
                             for (int i = 0; i < C::COLS_WARP; ++i)
                                 v[i] = __float_as_uint(fmaf(__uint_as_float(v[i]), args.alpha, b));
@@ -640,12 +719,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                             v[i] = __float_as_uint(activate(__uint_as_float(v[i]), args.act));
                     }
                 }
-                if (args.mode == kEpiRows || ra < args.rows_a) {       // the row stores are warp-collective
+                if (args.mode == kEpiRows || ra < tg.la) {             // the row stores are warp-collective
                     if (args.mode == kEpiRows) {
                         // D rows of this warp in 32-byte column chunks through the staging;
                         // SwiGLU stores half as many columns, from D column col0 / 2
                         const int oc0 = glu ? col0 >> 1 : col0;
-                        const int ocols = glu ? args.rows_b >> 1 : args.rows_b;
+                        const int ocols = glu ? tg.lb >> 1 : tg.lb;
                         const int nval = glu ? C::COLS_WARP / 2 : C::COLS_WARP;
                         if (args.bf16) {
 #pragma unroll
@@ -658,8 +737,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                                                  __uint_as_float(v[16 * ch + 2 * i + 1]));
                                         w[i] = *reinterpret_cast<uint32_t *>(&p);
                                     }
-                                    store_chunk32(stg_ptr, w, args.out, args.ldo, 2, row_base, oc0 + 16 * ch, 8,
-                                                  args.rows_a, ocols, lane, d_policy);
+                                    store_chunk32(stg_ptr, w, args.out, args.ldo, 2, tg.da + row_base, oc0 + 16 * ch, 8,
+                                                  tg.da + tg.la, ocols, lane, d_policy);
                                 }
                             }
                         } else {
@@ -669,8 +748,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     uint32_t w[8];
 #pragma unroll
                                     for (int i = 0; i < 8; ++i) w[i] = v[8 * ch + i];
-                                    store_chunk32(stg_ptr, w, args.out, args.ldo, 4, row_base, oc0 + 8 * ch, 4,
-                                                  args.rows_a, ocols, lane, d_policy);
+                                    store_chunk32(stg_ptr, w, args.out, args.ldo, 4, tg.da + row_base, oc0 + 8 * ch, 4,
+                                                  tg.da + tg.la, ocols, lane, d_policy);
                                 }
                             }
                         }
@@ -683,22 +762,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                             if (col0 + i < args.rows_b)
                                 st_global_b32_hint(ws + static_cast<int64_t>(col0 + i) * args.ldo, v[i], d_policy);
                     } else if (!glu || (lane & 1) == 0) {
-                        // D^T: this lane's GEMM column ra (SwiGLU: D column ra / 2, from the gate lane)
-                        const int oc = glu ? ra >> 1 : ra;
+                        // D^T: this lane's GEMM column ra (SwiGLU: D column ra / 2, from the gate
+                        // lane); D row db + (slot-B row)
+                        const int oc = tg.da + (glu ? ra >> 1 : ra);
+                        const int r0 = tg.db + col0;
                         if (args.bf16) {
                             __nv_bfloat16 *d = static_cast<__nv_bfloat16 *>(args.out) + oc;
 #pragma unroll
                             for (int i = 0; i < C::COLS_WARP; ++i)
-                                if (col0 + i < args.rows_b)
-                                    st_global_b16_hint(d + static_cast<int64_t>(col0 + i) * args.ldo,
+                                if (col0 + i < tg.lb)
+                                    st_global_b16_hint(d + static_cast<int64_t>(r0 + i) * args.ldo,
                                                        __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v[i]))),
                                                        d_policy);
                         } else {
                             float *d = static_cast<float *>(args.out) + oc;
 #pragma unroll
                             for (int i = 0; i < C::COLS_WARP; ++i)
-                                if (col0 + i < args.rows_b)
-                                    st_global_b32_hint(d + static_cast<int64_t>(col0 + i) * args.ldo, v[i], d_policy);
+                                if (col0 + i < tg.lb)
+                                    st_global_b32_hint(d + static_cast<int64_t>(r0 + i) * args.ldo, v[i], d_policy);
                         }
                     }
                 }
@@ -760,8 +841,11 @@ __global__ void splitk_reduce_kernel(const float *__restrict__ ws, void *__restr
 // (j = 0..3), columns 4cb..4cb+3 (zero past the matrix). A block of 256 threads
 // covers 8 consecutive atoms of one 128-row block, so its reads of a row fall
 // in one or two 32-byte sectors.
+// With `blocks` set (grouped GEMM), atom row-block rb holds the blocks[rb].y
+// rows starting at source row blocks[rb].x (each group's rows start a fresh
+// 128-row block); without it, rows rb*128 .. of a `rows`-row matrix.
 __global__ void scale_reorder_kernel(const uint8_t *__restrict__ sf, uint4 *__restrict__ out, int64_t rows,
-                                     int64_t ksf, int64_t kc4, int64_t lines)
+                                     int64_t ksf, int64_t kc4, int64_t lines, const int2 *__restrict__ blocks)
 {
     // 32-bit loads only when every row's 4-column group is 4-byte aligned
     const bool words = (ksf & 3) == 0 && (reinterpret_cast<uintptr_t>(sf) & 3) == 0;
@@ -771,12 +855,18 @@ __global__ void scale_reorder_kernel(const uint8_t *__restrict__ sf, uint4 *__re
         const int i = static_cast<int>(l & 31);
         const int64_t rb = atom / kc4, cb = atom - rb * kc4;
         const int64_t c0 = cb * 4;
+        int64_t src0 = rb * 128, valid = rows - rb * 128;
+        if (blocks) {
+            const int2 bt = __ldg(blocks + rb);
+            src0 = bt.x;
+            valid = bt.y;
+        }
         uint32_t w[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            const int64_t r = rb * 128 + 32 * j + i;
+            const int64_t r = src0 + 32 * j + i;
             uint32_t word = 0;
-            if (r < rows) {
+            if (32 * j + i < valid) {
                 const uint8_t *row = sf + r * ksf;
                 if (words) {
                     word = __ldg(reinterpret_cast<const uint32_t *>(row + c0));
@@ -801,7 +891,7 @@ int64_t g_wait_ms = -1;
 std::atomic<unsigned long long> g_epoch{0};   // per-launch value of the split-tail flags
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
-constexpr int kNumKernels = 14;   // kernel variants that can be launched (see kernel_index)
+constexpr int kNumKernels = 22;   // kernel variants that can be launched (see kernel_index)
 struct DeviceInfo {
     bool probed = false;
     bool ok = false;
@@ -900,12 +990,12 @@ struct Maps {
 
 // With `slots_out` set, only reports how many CTA groups a launch can keep
 // resident (after the cap) and launches nothing.
-template <int CG, int BN, bool MX>
+template <int CG, int BN, bool MX, bool GROUPED>
 cudaError_t launch_gemm(DeviceInfo &info, int kidx, int units, int cap, const Maps &m, const Args &args,
                         cudaStream_t stream, int *slots_out)
 {
     using C = Cfg<CG, BN, MX>;
-    auto kern = fp4_gemm_kernel<CG, BN, MX>;
+    auto kern = fp4_gemm_kernel<CG, BN, MX, GROUPED>;
     cudaLaunchAttribute cluster_attr[1];
     cluster_attr[0].id = cudaLaunchAttributeClusterDimension;
     cluster_attr[0].val.clusterDim.x = CG;
@@ -953,17 +1043,47 @@ cudaError_t launch_gemm(DeviceInfo &info, int kidx, int units, int cap, const Ma
 }
 
 // Variants: one CTA: N 16..256, pair: N 128 / 256; each for both formats.
-int kernel_index(int cg, int bn, bool mx)
+// Grouped: one CTA with N 64..256, or a pair with N 256.
+int kernel_index(int cg, int bn, bool mx, bool grouped = false)
 {
+    if (grouped) {
+        if (cg == 2) return bn == 256 ? 20 + (mx ? 1 : 0) : -1;                // 20..21
+        return bn >= 64 ? 14 + (bn_index(bn) - 2) * 2 + (mx ? 1 : 0) : -1;   // 14..19
+    }
     if (cg == 1) return bn_index(bn) * 2 + (mx ? 1 : 0);                   // 0..9
     return 10 + (bn == 256 ? 2 : 0) + (mx ? 1 : 0);                         // 10..13
+}
+
+cudaError_t launch_grouped(int cg, int bn, bool mx, DeviceInfo &info, int units, const Maps &m, const Args &args,
+                           cudaStream_t stream)
+{
+    const int k = kernel_index(cg, bn, mx, true);
+#define FP4_LAUNCH_G(CG_, BN_, MX_) return launch_gemm<CG_, BN_, MX_, true>(info, k, units, 0, m, args, stream, nullptr)
+    if (k < 0) return cudaErrorInvalidValue;
+    if (cg == 2) {
+        if (mx) FP4_LAUNCH_G(2, 256, true);
+        FP4_LAUNCH_G(2, 256, false);
+    }
+    switch (bn) {
+    case 64:
+        if (mx) FP4_LAUNCH_G(1, 64, true);
+        FP4_LAUNCH_G(1, 64, false);
+    case 128:
+        if (mx) FP4_LAUNCH_G(1, 128, true);
+        FP4_LAUNCH_G(1, 128, false);
+    default:
+        if (mx) FP4_LAUNCH_G(1, 256, true);
+        FP4_LAUNCH_G(1, 256, false);
+    }
+#undef FP4_LAUNCH_G
 }
 
 cudaError_t launch_by_cfg(int cg, int bn, bool mx, DeviceInfo &info, int units, int cap, const Maps &m,
                           const Args &args, cudaStream_t stream, int *slots_out = nullptr)
 {
     const int k = kernel_index(cg, bn, mx);
-#define FP4_LAUNCH(CG_, BN_, MX_) return launch_gemm<CG_, BN_, MX_>(info, k, units, cap, m, args, stream, slots_out)
+#define FP4_LAUNCH(CG_, BN_, MX_) \
+    return launch_gemm<CG_, BN_, MX_, false>(info, k, units, cap, m, args, stream, slots_out)
     if (cg == 2) {
         if (bn == 256) {
             if (mx) FP4_LAUNCH(2, 256, true);
@@ -1086,16 +1206,17 @@ fp4_status make_plan(int64_t M, int64_t N, int64_t K, bool rows_ok, bool mx, int
     return FP4_OK;
 }
 
+// `row_blocks` / `table`: the grouped form (table[rb] = first source row, rows).
 fp4_status reorder_launch(const void *sf_plain, void *sf_atom, int64_t rows, int64_t ksf, int sms,
-                          cudaStream_t stream)
+                          cudaStream_t stream, int64_t row_blocks = -1, const int2 *table = nullptr)
 {
     const int64_t kc4 = cdiv(ksf, 4);
-    const int64_t lines = cdiv(rows, 128) * kc4 * 32;
+    const int64_t lines = (table ? row_blocks : cdiv(rows, 128)) * kc4 * 32;
     if (lines == 0) return FP4_OK;
     const int threads = 256;
     const int64_t blocks = std::min<int64_t>(cdiv(lines, threads), static_cast<int64_t>(sms) * 32);
     scale_reorder_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
-        static_cast<const uint8_t *>(sf_plain), static_cast<uint4 *>(sf_atom), rows, ksf, kc4, lines);
+        static_cast<const uint8_t *>(sf_plain), static_cast<uint4 *>(sf_atom), rows, ksf, kc4, lines, table);
     return cudaGetLastError() == cudaSuccess ? FP4_OK : FP4_ERR_CUDA;
 }
 
@@ -1301,6 +1422,208 @@ fp4_status gemm_impl(fp4_format fmt, int prepacked, const void *A, const void *s
     return result;
 }
 
+// Grouped GEMM: one persistent launch over every group's tiles (GroupGeo).
+fp4_status grouped_impl(fp4_format fmt, int prepacked, int64_t G, const int64_t *offsets, const void *A,
+                        const void *sfA, const void *B, const void *sfB, float alpha, const fp4_epilogue *epi,
+                        void *D, int64_t N, int64_t K, fp4_out_dtype out, const fp4_gemm_config *cfg,
+                        cudaStream_t stream)
+{
+    if (fmt != FP4_FMT_NVFP4 && fmt != FP4_FMT_MXFP4) return FP4_ERR_INVALID_ARG;
+    if (out != FP4_OUT_F32 && out != FP4_OUT_BF16) return FP4_ERR_INVALID_ARG;
+    const int act = epi ? epi->act : FP4_ACT_NONE;
+    const float *bias = epi ? epi->bias : nullptr;
+    if (act < FP4_ACT_NONE || act > FP4_ACT_SWIGLU) return FP4_ERR_INVALID_ARG;
+    if (G < 0 || N < 0 || K < 0) return FP4_ERR_INVALID_ARG;
+    if (G == 0) return FP4_OK;
+    if (!offsets || offsets[0] != 0) return FP4_ERR_INVALID_ARG;
+    int64_t max_rows = 0;
+    for (int64_t g = 0; g < G; ++g) {
+        if (offsets[g + 1] < offsets[g]) return FP4_ERR_INVALID_ARG;
+        max_rows = std::max(max_rows, offsets[g + 1] - offsets[g]);
+    }
+    const int64_t M = offsets[G];
+    const bool glu = act == FP4_ACT_SWIGLU;
+    if (glu && N % 2 != 0) return FP4_ERR_UNSUPPORTED;
+    if (M == 0 || N == 0) return FP4_OK;
+    if (!D) return FP4_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(bias) & 3u) return FP4_ERR_MISALIGNED;
+    const int mode = cfg ? cfg->mode : 0;
+    if (mode < 0 || mode > 2) return FP4_ERR_INVALID_ARG;
+    if (cfg && (cfg->bn || cfg->splits > 1 || cfg->cta_group || cfg->max_ctas)) return FP4_ERR_UNSUPPORTED;
+    const int64_t esize = out == FP4_OUT_BF16 ? 2 : 4;
+    const int64_t d_cols = glu ? N / 2 : N;
+    if (K == 0) {
+        if (!aligned16(D)) return FP4_ERR_MISALIGNED;
+        if (act == FP4_ACT_NONE && !bias)
+            return cudaMemsetAsync(D, 0, static_cast<size_t>(M * d_cols * esize), stream) == cudaSuccess
+                       ? FP4_OK
+                       : FP4_ERR_CUDA;
+        if (M > (1ll << 30) || G * N > (1ll << 30)) return FP4_ERR_UNSUPPORTED;
+        int dev;
+        DeviceInfo *info;
+        const fp4_status st = device_info(dev, info);
+        if (st != FP4_OK) return st;
+        // D = epilogue(bias of the row's group), group by group (the split-K reduce with no partials)
+        for (int64_t g = 0; g < G; ++g) {
+            const int64_t m = offsets[g + 1] - offsets[g];
+            if (m == 0) continue;
+            const int64_t blocks = std::min<int64_t>(cdiv(m * d_cols, 256), static_cast<int64_t>(info->sms) * 8);
+            splitk_reduce_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+                nullptr, static_cast<uint8_t *>(D) + offsets[g] * d_cols * esize, m, N, d_cols, 0, 0, alpha,
+                out == FP4_OUT_BF16, bias ? bias + g * N : nullptr, act);
+            if (cudaGetLastError() != cudaSuccess) return FP4_ERR_CUDA;
+        }
+        return FP4_OK;
+    }
+    if (!A || !B || !sfA || !sfB) return FP4_ERR_INVALID_ARG;
+    if (K % 32 != 0) return FP4_ERR_UNSUPPORTED;
+    if (M > (1ll << 30) || G * N > (1ll << 30) || K > (1ll << 30) || M * N > (1ll << 46)) return FP4_ERR_UNSUPPORTED;
+    if (!aligned16(A) || !aligned16(B) || !aligned16(D)) return FP4_ERR_MISALIGNED;
+    if (prepacked & ~3) return FP4_ERR_INVALID_ARG;
+    const bool b_pre = prepacked & FP4_GROUPED_B_ATOMS, a_pre = prepacked & FP4_GROUPED_A_ATOMS;
+    if ((b_pre && !aligned16(sfB)) || (a_pre && !aligned16(sfA))) return FP4_ERR_MISALIGNED;
+
+    int dev;
+    DeviceInfo *info;
+    fp4_status st = device_info(dev, info);
+    if (st != FP4_OK) return st;
+    const bool mx = fmt == FP4_FMT_MXFP4;
+    const int vec = mx ? 32 : 16;
+    const int64_t ksf = K / vec, kc4 = cdiv(ksf, 4);
+    const bool rows_ok = (d_cols * esize) % 16 == 0;
+    const bool swap = mode == 2 || (mode == 0 && (max_rows <= 256 || !rows_ok));
+    if (!swap && !rows_ok) return FP4_ERR_MISALIGNED;
+    // swap-AB: one CTA per 128 weight rows, a group's rows in N tiles of BN (one
+    // tile when every group fits); direct: N tiles of 256, CTA pairs for MXFP4
+    const int bn = swap ? std::max(64, pow2_bn(std::min<int64_t>(max_rows, 256))) : 256;
+    const int cg = swap ? 1 : (mx ? 2 : 1);
+    const int nrb = static_cast<int>(cdiv(bn, 128));
+    const int64_t nb = cdiv(N, 128);                 // scale blocks of one B_g
+
+    // host tables: A's scale blocks (each group starts a fresh 128-row block),
+    // B's (when reordered here), unit -> group, per-group geometry
+    std::vector<int2> a_blocks, b_blocks;
+    std::vector<GroupGeo> geo(static_cast<size_t>(G));
+    std::vector<int32_t> unit_group;
+    for (int64_t g = 0; g < G; ++g) {
+        const int64_t m = offsets[g + 1] - offsets[g];
+        const int64_t blk0 = static_cast<int64_t>(a_blocks.size());
+        for (int64_t b = 0; b < cdiv(m, 128); ++b)
+            a_blocks.push_back(make_int2(static_cast<int>(offsets[g] + 128 * b),
+                                         static_cast<int>(std::min<int64_t>(128, m - 128 * b))));
+        GroupGeo &q = geo[static_cast<size_t>(g)];
+        std::memset(&q, 0, sizeof q);
+        q.first = static_cast<int32_t>(unit_group.size());
+        q.bias_off = static_cast<int32_t>(g * N);
+        int64_t units_g;
+        if (swap) {
+            q.tiles_a = static_cast<int32_t>(cdiv(N, 128));
+            q.oa = static_cast<int32_t>(g * N), q.sa = static_cast<int32_t>(g * nb), q.da = 0,
+            q.la = static_cast<int32_t>(N);
+            q.ob = static_cast<int32_t>(offsets[g]), q.sb = static_cast<int32_t>(blk0),
+            q.db = static_cast<int32_t>(offsets[g]), q.lb = static_cast<int32_t>(m);
+            units_g = q.tiles_a * cdiv(m, bn);
+        } else {
+            q.tiles_a = static_cast<int32_t>(cdiv(m, 128 * cg));
+            q.oa = static_cast<int32_t>(offsets[g]), q.sa = static_cast<int32_t>(blk0),
+            q.da = static_cast<int32_t>(offsets[g]), q.la = static_cast<int32_t>(m);
+            q.ob = static_cast<int32_t>(g * N), q.sb = static_cast<int32_t>(g * nb), q.db = 0,
+            q.lb = static_cast<int32_t>(N);
+            units_g = q.tiles_a * cdiv(N, bn);
+        }
+        unit_group.insert(unit_group.end(), static_cast<size_t>(units_g), static_cast<int32_t>(g));
+    }
+    if (!b_pre)
+        for (int64_t g = 0; g < G; ++g)
+            for (int64_t b = 0; b < nb; ++b)
+                b_blocks.push_back(make_int2(static_cast<int>(g * N + 128 * b),
+                                             static_cast<int>(std::min<int64_t>(128, N - 128 * b))));
+    const int64_t units = static_cast<int64_t>(unit_group.size());
+    if (units > (1ll << 30)) return FP4_ERR_UNSUPPORTED;
+
+    // scratch: [A atoms][B atoms][tables], each 256-byte aligned
+    auto up = [](size_t b) { return (b + 255) & ~static_cast<size_t>(255); };
+    const int64_t a_nblk = static_cast<int64_t>(a_blocks.size());
+    const size_t atoms_a = a_pre ? 0 : static_cast<size_t>(a_nblk * kc4 * kAtomBytes);
+    const size_t atoms_b = b_pre ? 0 : static_cast<size_t>(G * nb * kc4 * kAtomBytes);
+    const size_t t_ablk = a_blocks.size() * sizeof(int2), t_bblk = b_blocks.size() * sizeof(int2);
+    const size_t t_units = unit_group.size() * sizeof(int32_t), t_geo = geo.size() * sizeof(GroupGeo);
+    const size_t off_b = up(atoms_a), off_tab = off_b + up(atoms_b);
+    const size_t off_bblk = up(t_ablk), off_units = off_bblk + up(t_bblk), off_geo = off_units + up(t_units);
+    const size_t tab_bytes = off_geo + up(t_geo);
+    std::vector<uint8_t> host_tab(tab_bytes, 0);
+    std::memcpy(host_tab.data(), a_blocks.data(), t_ablk);
+    if (t_bblk) std::memcpy(host_tab.data() + off_bblk, b_blocks.data(), t_bblk);
+    std::memcpy(host_tab.data() + off_units, unit_group.data(), t_units);
+    std::memcpy(host_tab.data() + off_geo, geo.data(), t_geo);
+    uint8_t *scratch = nullptr;
+    if (cudaMallocAsync(reinterpret_cast<void **>(&scratch), off_tab + tab_bytes, stream) != cudaSuccess)
+        return FP4_ERR_CUDA;
+    fp4_status result = FP4_OK;
+    do {
+        uint8_t *tab = scratch + off_tab;
+        // pageable source: the call returns once the bytes are staged, so the
+        // host vector may go out of scope
+        if (cudaMemcpyAsync(tab, host_tab.data(), tab_bytes, cudaMemcpyHostToDevice, stream) != cudaSuccess) {
+            result = FP4_ERR_CUDA;
+            break;
+        }
+        const uint8_t *a_atoms = static_cast<const uint8_t *>(sfA);
+        const uint8_t *b_atoms = static_cast<const uint8_t *>(sfB);
+        if (!a_pre) {
+            if ((result = reorder_launch(sfA, scratch, M, ksf, info->sms, stream, a_nblk,
+                                         reinterpret_cast<const int2 *>(tab))) != FP4_OK)
+                break;
+            a_atoms = scratch;
+        }
+        if (!b_pre) {
+            if ((result = reorder_launch(sfB, scratch + off_b, G * N, ksf, info->sms, stream, G * nb,
+                                         reinterpret_cast<const int2 *>(tab + off_bblk))) != FP4_OK)
+                break;
+            b_atoms = scratch + off_b;
+        }
+        const int apk = mx ? 2 : 4;
+        Maps m;
+        std::memset(&m, 0, sizeof m);
+        const bool ok = swap ? (encode_operand(&m.a, B, G * N, K, kBM) && encode_operand(&m.b, A, M, K, bn) &&
+                                encode_scales(&m.sfa, b_atoms, G * nb, kc4, apk, 1) &&
+                                encode_scales(&m.sfb, a_atoms, a_nblk, kc4, apk, nrb))
+                             : (encode_operand(&m.a, A, M, K, kBM) && encode_operand(&m.b, B, G * N, K, bn / cg) &&
+                                encode_scales(&m.sfa, a_atoms, a_nblk, kc4, apk, 1) &&
+                                encode_scales(&m.sfb, b_atoms, G * nb, kc4, apk, nrb));
+        if (!ok) {
+            result = FP4_ERR_CUDA;
+            break;
+        }
+        Args a;
+        std::memset(&a, 0, sizeof a);
+        a.wait_ns = wait_limit_ns();
+        a.rows_a = static_cast<int32_t>(swap ? N : M);
+        a.rows_b = static_cast<int32_t>(swap ? M : N);
+        a.k_tiles = static_cast<int32_t>(cdiv(K, kBK));
+        a.kps = a.k_tiles;
+        a.splits = 1;
+        a.tiles_a = a.tiles_b = 1;
+        a.units = static_cast<int32_t>(units);
+        a.group_b = 1;
+        a.bf16 = out == FP4_OUT_BF16;
+        a.mode = swap ? kEpiTransposed : kEpiRows;
+        a.act = act;
+        a.alpha = alpha;
+        a.bias = bias;
+        a.out = D;
+        a.ldo = d_cols;
+        a.split_units = 0;
+        a.unit_group = reinterpret_cast<const int32_t *>(tab + off_units);
+        a.geo = reinterpret_cast<const GroupGeo *>(tab + off_geo);
+        a.epoch = ++g_epoch;
+        if (units > 0 && launch_grouped(cg, bn, mx, *info, static_cast<int>(units), m, a, stream) != cudaSuccess)
+            result = FP4_ERR_CUDA;
+    } while (false);
+    if (cudaFreeAsync(scratch, stream) != cudaSuccess && result == FP4_OK) result = FP4_ERR_CUDA;
+    return result;
+}
+
 // Device address of g_static_scratch on device `dev`, looked up once per
 // device (with that device current) and kept.
 uint8_t *g_static_scratch_addr[64] = {};
@@ -1367,6 +1690,60 @@ fp4_status fp4_gemm_plan(fp4_format fmt, int scales_prepacked, int64_t M, int64_
     info->splits = static_cast<int32_t>(cdiv(cdiv(K, kBK), cdiv(cdiv(K, kBK), plan.splits)));
     info->launches = (scales_prepacked ? 0 : 2) + 1 + (info->splits > 1 ? 1 : 0);
     return FP4_OK;
+}
+
+fp4_status fp4_gemm_grouped(fp4_format fmt, int weights_prepacked, int64_t G, const int64_t *offsets,
+                            const void *A, const void *sfA, const void *B, const void *sfB, float alpha,
+                            const fp4_epilogue *epi, void *D, int64_t N, int64_t K, fp4_out_dtype out,
+                            const fp4_gemm_config *cfg, cudaStream_t stream)
+{
+    return grouped_impl(fmt, weights_prepacked, G, offsets, A, sfA, B, sfB, alpha, epi, D, N, K, out, cfg, stream);
+}
+
+size_t fp4_scale_atom_bytes_grouped(int64_t G, const int64_t *offsets, int64_t k, int vec)
+{
+    if (G < 0 || k < 0 || (vec != 16 && vec != 32) || k % vec != 0 || (G > 0 && !offsets)) return 0;
+    int64_t blocks = 0;
+    for (int64_t g = 0; g < G; ++g) {
+        if (offsets[g + 1] < offsets[g]) return 0;
+        blocks += cdiv(offsets[g + 1] - offsets[g], 128);
+    }
+    return static_cast<size_t>(blocks * cdiv(k / vec, 4) * kAtomBytes);
+}
+
+fp4_status fp4_scale_reorder_grouped(const void *sf_plain, void *sf_atom, int64_t G, const int64_t *offsets,
+                                     int64_t k, int vec, cudaStream_t stream)
+{
+    if (G < 0 || k < 0 || (vec != 16 && vec != 32)) return FP4_ERR_INVALID_ARG;
+    if (k % vec != 0) return FP4_ERR_UNSUPPORTED;
+    if (G == 0 || k == 0) return FP4_OK;
+    if (!offsets || offsets[0] != 0) return FP4_ERR_INVALID_ARG;
+    std::vector<int2> blocks;
+    for (int64_t g = 0; g < G; ++g) {
+        const int64_t m = offsets[g + 1] - offsets[g];
+        if (m < 0) return FP4_ERR_INVALID_ARG;
+        for (int64_t b = 0; b < cdiv(m, 128); ++b)
+            blocks.push_back(make_int2(static_cast<int>(offsets[g] + 128 * b),
+                                       static_cast<int>(std::min<int64_t>(128, m - 128 * b))));
+    }
+    if (offsets[G] > (1ll << 30)) return FP4_ERR_UNSUPPORTED;
+    if (blocks.empty()) return FP4_OK;
+    if (!sf_plain || !sf_atom) return FP4_ERR_INVALID_ARG;
+    if (!aligned16(sf_atom)) return FP4_ERR_MISALIGNED;
+    int dev;
+    DeviceInfo *info;
+    fp4_status st = device_info(dev, info);
+    if (st != FP4_OK) return st;
+    const size_t bytes = blocks.size() * sizeof(int2);
+    int2 *table = nullptr;
+    if (cudaMallocAsync(reinterpret_cast<void **>(&table), bytes, stream) != cudaSuccess) return FP4_ERR_CUDA;
+    if (cudaMemcpyAsync(table, blocks.data(), bytes, cudaMemcpyHostToDevice, stream) != cudaSuccess)
+        st = FP4_ERR_CUDA;
+    if (st == FP4_OK)
+        st = reorder_launch(sf_plain, sf_atom, offsets[G], k / vec, info->sms, stream,
+                            static_cast<int64_t>(blocks.size()), table);
+    if (cudaFreeAsync(table, stream) != cudaSuccess && st == FP4_OK) st = FP4_ERR_CUDA;
+    return st;
 }
 
 fp4_status fp4_gemm_fused(fp4_format fmt, int scales_prepacked, const void *A, const void *sfA, const void *B,

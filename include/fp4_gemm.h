@@ -179,6 +179,47 @@ fp4_status fp4_gemm_fused(fp4_format fmt, int scales_prepacked, const void *A, c
                           void *D, int64_t M, int64_t N, int64_t K, fp4_out_dtype out,
                           const fp4_gemm_config *cfg, cudaStream_t stream);
 
+/* Grouped GEMM (a mixture-of-experts layer): G independent GEMMs sharing N
+ * and K. Group g owns rows offsets[g] .. offsets[g+1]-1 of A and of D and the
+ * weight matrix B_g; for each g
+ *   D[offsets[g] + i][n] = epi( alpha * sum_k a(offsets[g] + i, k) * b_g(n, k) + bias[g*N + n] )
+ * (the NVFP4 ReLU-squared MoE of "TMA Pipelines, Tensor Cores, and ctm-rs
+ * Interop", "Where to Go Next": each expert's weights applied to the tokens
+ * routed to it, rows sorted by expert).
+ *   offsets  HOST array of G+1 int64: offsets[0] = 0, non-decreasing (empty
+ *            groups allowed), M_total = offsets[G]. Read during the call only.
+ *   A        [M_total][K/2], sfA plain [M_total][K/vec].
+ *   B        [G][N][K/2] (B_g contiguous); sfB plain [G][N][K/vec], or with
+ *            FP4_GROUPED_B_ATOMS in scales_prepacked the G atom-layout copies
+ *            of fp4_scale_reorder back to back (each fp4_scale_atom_bytes(N,
+ *            K, vec) bytes; the same bytes as one reorder of all G*N rows
+ *            when N % 128 == 0). With FP4_GROUPED_A_ATOMS, sfA is the output
+ *            of fp4_scale_reorder_grouped for the same offsets.
+ *   epi      as fp4_gemm_fused; bias, if given, is [G][N] floats (per group).
+ *   D        [M_total][N] (or [M_total][N/2] for SwiGLU).
+ * One launch covers every group: the persistent kernel's tiles are the groups'
+ * tiles back to back. Plan: swap-AB (weights on the MMA's M side, one tile of
+ * a group's rows on its N side) when every group has at most 256 rows or D's
+ * rows cannot take 16-byte stores, else direct; no K split. Scratch:
+ * stream-ordered (the reordered scales and small per-group tables).
+ * Requirements and errors as fp4_gemm; offsets not starting at 0 or
+ * decreasing give FP4_ERR_INVALID_ARG; M_total or G * N above 2^30,
+ * FP4_ERR_UNSUPPORTED. cfg may force mode 1 (direct) or 2 (swap-AB). */
+#define FP4_GROUPED_B_ATOMS 1   /* sfB: the G groups' atom-layout copies back to back */
+#define FP4_GROUPED_A_ATOMS 2   /* sfA: the grouped atom layout of fp4_scale_reorder_grouped */
+fp4_status fp4_gemm_grouped(fp4_format fmt, int scales_prepacked, int64_t G, const int64_t *offsets,
+                            const void *A, const void *sfA, const void *B, const void *sfB, float alpha,
+                            const fp4_epilogue *epi, void *D, int64_t N, int64_t K, fp4_out_dtype out,
+                            const fp4_gemm_config *cfg, cudaStream_t stream);
+
+/* The grouped atom layout of activation scales: each group's rows
+ * (offsets as fp4_gemm_grouped) reordered like fp4_scale_reorder, every group
+ * starting a fresh 128-row block; fp4_scale_atom_bytes_grouped gives its size
+ * (0 for invalid arguments). Host offsets; errors as fp4_scale_reorder. */
+size_t fp4_scale_atom_bytes_grouped(int64_t G, const int64_t *offsets, int64_t k, int vec);
+fp4_status fp4_scale_reorder_grouped(const void *sf_plain, void *sf_atom, int64_t G, const int64_t *offsets,
+                                     int64_t k, int vec, cudaStream_t stream);
+
 /* Host-buffer convenience form: A, sfA, B, sfB and D live in HOST memory
  * (pinned for asynchronous copies). The call copies the inputs to stream-ordered
  * device scratch, runs fp4_gemm, copies D back and returns; D is valid once

@@ -135,6 +135,33 @@ def test_plan_host_validation_without_device(fp4):
     assert plan(cfg=ctypes.byref(fp4.GemmConfig(mode=4))) in (1, 6)   # bad mode (or no device first)
 
 
+def test_grouped_host_validation_without_device(fp4):
+    buf = np.zeros(4096 + 16, np.uint8)
+    p = buf.ctypes.data + (-buf.ctypes.data) % 16
+    lib = fp4.load()
+
+    def grp(offs, N=64, K=64, act=0, bias=None, fmt=0, out=0, cfg=None, D=None):
+        o = np.ascontiguousarray(offs, dtype=np.int64)
+        epi = fp4.Epilogue(act, bias)
+        return lib.fp4_gemm_grouped(fmt, 0, o.size - 1, o.ctypes.data if o.size else None, p, p, p, p, 1.0,
+                                    ctypes.byref(epi), p if D is None else D, N, K, out, cfg, 0)
+
+    assert lib.fp4_gemm_grouped(0, 0, 0, None, p, p, p, p, 1.0, None, p, 64, 64, 0, None, 0) == 0   # G = 0
+    assert grp([0, 0, 0]) == 0                      # every group empty
+    assert grp([0, 4, 9], N=0) == 0
+    assert grp([1, 4]) == 1                         # offsets[0] != 0
+    assert grp([0, 5, 4]) == 1                      # decreasing
+    assert grp([0, 4], fmt=2) == 1
+    assert grp([0, 4], act=7) == 1
+    assert grp([0, 4], N=63, act=3) == 2            # SwiGLU, odd N
+    assert grp([0, 4], bias=p + 2, act=1) == 3      # misaligned bias
+    assert grp([0, 4], K=48) == 2
+    assert grp([0, 4], D=p + 8) == 3                # misaligned D
+    assert grp([0, 4], cfg=ctypes.byref(fp4.GemmConfig(mode=5))) == 1
+    assert grp([0, 4], cfg=ctypes.byref(fp4.GemmConfig(splits=2))) == 2
+    assert lib.fp4_gemm_grouped(0, 0, 2, None, p, p, p, p, 1.0, None, p, 64, 64, 0, None, 0) == 1   # no offsets
+
+
 def test_quantize_host_validation_without_device(fp4):
     buf = np.zeros(4096 + 16, np.uint8)
     p = buf.ctypes.data + (-buf.ctypes.data) % 16
@@ -169,3 +196,13 @@ def test_package_fails_loudly_without_library(tmp_path, monkeypatch):
     monkeypatch.setattr(m._build, "LIB", str(tmp_path / "missing.so"))
     with pytest.raises(ImportError):
         m.load()
+
+
+def test_grouped_atom_bytes_without_device(fp4):
+    import oracle
+    offsets = np.array([0, 130, 130, 131, 400], np.int64)
+    want = sum(oracle.scale_atom_bytes(int(b - a), 256 // 16) for a, b in zip(offsets[:-1], offsets[1:]) if b > a)
+    assert fp4.scale_atom_bytes_grouped(offsets, 256, 16) == want
+    assert fp4.scale_atom_bytes_grouped([0, 5, 3], 256, 16) == 0        # decreasing
+    assert fp4.scale_atom_bytes_grouped([0, 5], 48, 32) == 0            # K % vec
+    assert fp4.scale_atom_bytes_grouped([0], 256, 16) == 0              # no groups
