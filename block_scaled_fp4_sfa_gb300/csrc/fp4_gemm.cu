@@ -94,6 +94,16 @@ struct GroupGeo {
 };
 static_assert(sizeof(GroupGeo) == 48, "three 16-byte loads");
 
+// The groups travel in the grouped kernel's parameter block (constant memory,
+// read with a uniform index): no table upload, so no host-side stream
+// synchronisation, per call.
+constexpr int kMaxGroups = 256;
+struct GroupParams {
+    int32_t count;
+    int32_t pad[3];
+    GroupGeo g[kMaxGroups];
+};
+
 // A unit's tile and where it sits (the whole problem when not grouped).
 struct TileGeo {
     int ta, tb;
@@ -123,17 +133,8 @@ struct Args {
     // the second half adds it.
     int32_t split_units;
     int32_t kh;                          // k-tiles of a first half
-    union {                              // (the parameter block keeps its size: a larger one
-                                         // costs the widest variants a register spill)
-        struct {                         // split tail
-            float *tail_ws;              // [tail tile][CTA of the pair][BN][128]
-            unsigned long long *tail_flags;   // [tail tile][CTA of the pair]
-        };
-        struct {                         // grouped kernels: unit -> group, each group's geometry
-            const int32_t *unit_group;
-            const GroupGeo *geo;
-        };
-    };
+    float *tail_ws;                      // [tail tile][CTA of the pair][BN][128]
+    unsigned long long *tail_flags;      // [tail tile][CTA of the pair]
     unsigned long long epoch;            // this launch's flag value
 };
 
@@ -296,24 +297,28 @@ __device__ __forceinline__ void unit_coords(const Args &a, int u, int &ta, int &
 
 // Where unit u's tile sits; ta / tb as unit_work gives them when not grouped.
 template <bool GROUPED>
-__device__ __forceinline__ void tile_geo(const Args &a, int u, int ta, int tb, TileGeo &t)
+__device__ __forceinline__ void tile_geo(const Args &a, const GroupParams *gp, int u, int ta, int tb, TileGeo &t)
 {
     if constexpr (GROUPED) {
-        const int g = __ldg(a.unit_group + u);
-        const int4 *p = reinterpret_cast<const int4 *>(a.geo + g);
-        const int4 w0 = __ldg(p), w1 = __ldg(p + 1), w2 = __ldg(p + 2);
-        const int lu = u - w0.x;
-        t.tb = lu / w0.y;
-        t.ta = lu - t.tb * w0.y;
-        t.oa = w0.z;
-        t.sa = w0.w;
-        t.da = w1.x;
-        t.la = w1.y;
-        t.ob = w1.z;
-        t.sb = w1.w;
-        t.db = w2.x;
-        t.lb = w2.y;
-        t.bias_off = w2.z;
+        // the last group whose first unit is <= u (empty groups share a first)
+        int lo = 0, hi = gp->count - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (gp->g[mid].first <= u) lo = mid; else hi = mid - 1;
+        }
+        const GroupGeo &q = gp->g[lo];
+        const int lu = u - q.first;
+        t.tb = lu / q.tiles_a;
+        t.ta = lu - t.tb * q.tiles_a;
+        t.oa = q.oa;
+        t.sa = q.sa;
+        t.da = q.da;
+        t.la = q.la;
+        t.ob = q.ob;
+        t.sb = q.sb;
+        t.db = q.db;
+        t.lb = q.lb;
+        t.bias_off = q.bias_off;
         return;
     }
     else {
@@ -402,10 +407,9 @@ __device__ __forceinline__ void store_chunk32(uint8_t *stg, const uint32_t (&w)[
 }
 
 template <int CG, int BN, bool MX, bool GROUPED>
-__global__ void __launch_bounds__(kThreads, 1)
-    fp4_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
-                    const __grid_constant__ CUtensorMap tmap_sfa, const __grid_constant__ CUtensorMap tmap_sfb,
-                    const Args args)
+__device__ __forceinline__ void gemm_body(const CUtensorMap &tmap_a, const CUtensorMap &tmap_b,
+                                          const CUtensorMap &tmap_sfa, const CUtensorMap &tmap_sfb, const Args &args,
+                                          const GroupParams *gp)
 {
     using C = Cfg<CG, BN, MX>;
     extern __shared__ uint8_t smem_raw[];
@@ -473,7 +477,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 int ta, tb, split, kt0, kt1, half, tidx;
                 unit_work<GROUPED>(args, u, ta, tb, split, kt0, kt1, half, tidx);
                 TileGeo tg;
-                tile_geo<GROUPED>(args, u, ta, tb, tg);
+                tile_geo<GROUPED>(args, gp, u, ta, tb, tg);
                 const int rba = tg.ta * CG + static_cast<int>(rank);     // this CTA's 128-row block of slot A
                 const int row_a = tg.oa + rba * kBM;
                 const int row_b = tg.ob + tg.tb * BN + static_cast<int>(rank) * C::BN_CTA;
@@ -624,7 +628,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             int ta, tb, split, kt0, kt1, half, tidx;
             unit_work<GROUPED>(args, u, ta, tb, split, kt0, kt1, half, tidx);
             TileGeo tg;
-            tile_geo<GROUPED>(args, u, ta, tb, tg);
+            tile_geo<GROUPED>(args, gp, u, ta, tb, tg);
             if (!wait(bar_acc_full + 8 * acc, acc_phase, args.wait_ns, abort_flag)) break;
             tc_fence_after();
             // Drain this warp's 32 lanes x BN/2 columns, then release the accumulator.
@@ -800,6 +804,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 1) tmem_dealloc<CG>(tmem, C::TMEM_COLS);
 }
 
+template <int CG, int BN, bool MX>
+__global__ void __launch_bounds__(kThreads, 1)
+    fp4_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
+                    const __grid_constant__ CUtensorMap tmap_sfa, const __grid_constant__ CUtensorMap tmap_sfb,
+                    const Args args)
+{
+    gemm_body<CG, BN, MX, false>(tmap_a, tmap_b, tmap_sfa, tmap_sfb, args, nullptr);
+}
+
+template <int CG, int BN, bool MX>
+__global__ void __launch_bounds__(kThreads, 1)
+    fp4_gemm_grouped_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
+                            const __grid_constant__ CUtensorMap tmap_sfa, const __grid_constant__ CUtensorMap tmap_sfb,
+                            const Args args, const __grid_constant__ GroupParams groups)
+{
+    gemm_body<CG, BN, MX, true>(tmap_a, tmap_b, tmap_sfa, tmap_sfb, args, &groups);
+}
+
 // Split-K: z[rb][ra] = alpha * sum_s ws[s][rb][ra] (+ bias[ra]) in a fixed
 // order (deterministic), then the fused epilogue into D[rb][.]. With splits = 0
 // (K = 0) z is the bias alone.
@@ -841,11 +863,19 @@ __global__ void splitk_reduce_kernel(const float *__restrict__ ws, void *__restr
 // (j = 0..3), columns 4cb..4cb+3 (zero past the matrix). A block of 256 threads
 // covers 8 consecutive atoms of one 128-row block, so its reads of a row fall
 // in one or two 32-byte sectors.
-// With `blocks` set (grouped GEMM), atom row-block rb holds the blocks[rb].y
-// rows starting at source row blocks[rb].x (each group's rows start a fresh
-// 128-row block); without it, rows rb*128 .. of a `rows`-row matrix.
+// Which source rows an atom row-block holds. Plain (groups == 0): block rb
+// holds rows rb*128 .. of a `rows`-row matrix. Grouped (each group's rows start
+// a fresh 128-row block): every group `uniform` rows (uniform > 0), or group g
+// = rows row0[g] .. row0[g+1]-1 starting at block first_blk[g].
+struct RowBlocks {
+    int32_t groups;
+    int32_t uniform;
+    int32_t first_blk[kMaxGroups + 1];
+    int32_t row0[kMaxGroups + 1];
+};
+
 __global__ void scale_reorder_kernel(const uint8_t *__restrict__ sf, uint4 *__restrict__ out, int64_t rows,
-                                     int64_t ksf, int64_t kc4, int64_t lines, const int2 *__restrict__ blocks)
+                                     int64_t ksf, int64_t kc4, int64_t lines, const __grid_constant__ RowBlocks rbm)
 {
     // 32-bit loads only when every row's 4-column group is 4-byte aligned
     const bool words = (ksf & 3) == 0 && (reinterpret_cast<uintptr_t>(sf) & 3) == 0;
@@ -856,10 +886,20 @@ __global__ void scale_reorder_kernel(const uint8_t *__restrict__ sf, uint4 *__re
         const int64_t rb = atom / kc4, cb = atom - rb * kc4;
         const int64_t c0 = cb * 4;
         int64_t src0 = rb * 128, valid = rows - rb * 128;
-        if (blocks) {
-            const int2 bt = __ldg(blocks + rb);
-            src0 = bt.x;
-            valid = bt.y;
+        if (rbm.groups > 0 && rbm.uniform > 0) {
+            const int64_t per = (rbm.uniform + 127) / 128;
+            const int64_t g = rb / per, b = rb - g * per;
+            src0 = g * rbm.uniform + 128 * b;
+            valid = rbm.uniform - 128 * b;
+        } else if (rbm.groups > 0) {
+            int lo = 0, hi = rbm.groups - 1;          // the last group starting at or before rb
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if (rbm.first_blk[mid] <= rb) lo = mid; else hi = mid - 1;
+            }
+            const int64_t b = rb - rbm.first_blk[lo];
+            src0 = rbm.row0[lo] + 128 * b;
+            valid = rbm.row0[lo + 1] - rbm.row0[lo] - 128 * b;
         }
         uint32_t w[4];
 #pragma unroll
@@ -992,10 +1032,13 @@ struct Maps {
 // resident (after the cap) and launches nothing.
 template <int CG, int BN, bool MX, bool GROUPED>
 cudaError_t launch_gemm(DeviceInfo &info, int kidx, int units, int cap, const Maps &m, const Args &args,
-                        cudaStream_t stream, int *slots_out)
+                        cudaStream_t stream, int *slots_out, const GroupParams *gp = nullptr)
 {
     using C = Cfg<CG, BN, MX>;
-    auto kern = fp4_gemm_kernel<CG, BN, MX, GROUPED>;
+    auto kern = [] {
+        if constexpr (GROUPED) return fp4_gemm_grouped_kernel<CG, BN, MX>;
+        else return fp4_gemm_kernel<CG, BN, MX>;
+    }();
     cudaLaunchAttribute cluster_attr[1];
     cluster_attr[0].id = cudaLaunchAttributeClusterDimension;
     cluster_attr[0].val.clusterDim.x = CG;
@@ -1039,7 +1082,10 @@ cudaError_t launch_gemm(DeviceInfo &info, int kidx, int units, int cap, const Ma
         lc.attrs = cluster_attr;
         lc.numAttrs = 1;
     }
-    return cudaLaunchKernelEx(&lc, kern, m.a, m.b, m.sfa, m.sfb, args);
+    if constexpr (GROUPED)
+        return cudaLaunchKernelEx(&lc, kern, m.a, m.b, m.sfa, m.sfb, args, *gp);
+    else
+        return cudaLaunchKernelEx(&lc, kern, m.a, m.b, m.sfa, m.sfb, args);
 }
 
 // Variants: one CTA: N 16..256, pair: N 128 / 256; each for both formats.
@@ -1055,10 +1101,11 @@ int kernel_index(int cg, int bn, bool mx, bool grouped = false)
 }
 
 cudaError_t launch_grouped(int cg, int bn, bool mx, DeviceInfo &info, int units, const Maps &m, const Args &args,
-                           cudaStream_t stream)
+                           const GroupParams &gp, cudaStream_t stream)
 {
     const int k = kernel_index(cg, bn, mx, true);
-#define FP4_LAUNCH_G(CG_, BN_, MX_) return launch_gemm<CG_, BN_, MX_, true>(info, k, units, 0, m, args, stream, nullptr)
+#define FP4_LAUNCH_G(CG_, BN_, MX_) \
+    return launch_gemm<CG_, BN_, MX_, true>(info, k, units, 0, m, args, stream, nullptr, &gp)
     if (k < 0) return cudaErrorInvalidValue;
     if (cg == 2) {
         if (mx) FP4_LAUNCH_G(2, 256, true);
@@ -1206,17 +1253,19 @@ fp4_status make_plan(int64_t M, int64_t N, int64_t K, bool rows_ok, bool mx, int
     return FP4_OK;
 }
 
-// `row_blocks` / `table`: the grouped form (table[rb] = first source row, rows).
+// `row_blocks` / `rbm`: the grouped forms (see RowBlocks).
 fp4_status reorder_launch(const void *sf_plain, void *sf_atom, int64_t rows, int64_t ksf, int sms,
-                          cudaStream_t stream, int64_t row_blocks = -1, const int2 *table = nullptr)
+                          cudaStream_t stream, int64_t row_blocks = -1, const RowBlocks *rbm = nullptr)
 {
     const int64_t kc4 = cdiv(ksf, 4);
-    const int64_t lines = (table ? row_blocks : cdiv(rows, 128)) * kc4 * 32;
+    const int64_t lines = (rbm ? row_blocks : cdiv(rows, 128)) * kc4 * 32;
     if (lines == 0) return FP4_OK;
     const int threads = 256;
     const int64_t blocks = std::min<int64_t>(cdiv(lines, threads), static_cast<int64_t>(sms) * 32);
+    static const RowBlocks plain = {};
     scale_reorder_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
-        static_cast<const uint8_t *>(sf_plain), static_cast<uint4 *>(sf_atom), rows, ksf, kc4, lines, table);
+        static_cast<const uint8_t *>(sf_plain), static_cast<uint4 *>(sf_atom), rows, ksf, kc4, lines,
+        rbm ? *rbm : plain);
     return cudaGetLastError() == cudaSuccess ? FP4_OK : FP4_ERR_CUDA;
 }
 
@@ -1436,6 +1485,7 @@ fp4_status grouped_impl(fp4_format fmt, int prepacked, int64_t G, const int64_t 
     if (G < 0 || N < 0 || K < 0) return FP4_ERR_INVALID_ARG;
     if (G == 0) return FP4_OK;
     if (!offsets || offsets[0] != 0) return FP4_ERR_INVALID_ARG;
+    if (G > kMaxGroups) return FP4_ERR_UNSUPPORTED;
     int64_t max_rows = 0;
     for (int64_t g = 0; g < G; ++g) {
         if (offsets[g + 1] < offsets[g]) return FP4_ERR_INVALID_ARG;
@@ -1500,85 +1550,68 @@ fp4_status grouped_impl(fp4_format fmt, int prepacked, int64_t G, const int64_t 
     const int nrb = static_cast<int>(cdiv(bn, 128));
     const int64_t nb = cdiv(N, 128);                 // scale blocks of one B_g
 
-    // host tables: A's scale blocks (each group starts a fresh 128-row block),
-    // B's (when reordered here), unit -> group, per-group geometry
-    std::vector<int2> a_blocks, b_blocks;
-    std::vector<GroupGeo> geo(static_cast<size_t>(G));
-    std::vector<int32_t> unit_group;
+    // The groups' geometry (kernel parameters) and the row map of A's scale
+    // reorder (each group's rows start a fresh 128-row block)
+    GroupParams gp;
+    RowBlocks a_map;
+    std::memset(&gp, 0, sizeof gp);
+    std::memset(&a_map, 0, sizeof a_map);
+    gp.count = static_cast<int32_t>(G);
+    a_map.groups = static_cast<int32_t>(G);
+    int64_t units = 0, a_nblk = 0;
     for (int64_t g = 0; g < G; ++g) {
         const int64_t m = offsets[g + 1] - offsets[g];
-        const int64_t blk0 = static_cast<int64_t>(a_blocks.size());
-        for (int64_t b = 0; b < cdiv(m, 128); ++b)
-            a_blocks.push_back(make_int2(static_cast<int>(offsets[g] + 128 * b),
-                                         static_cast<int>(std::min<int64_t>(128, m - 128 * b))));
-        GroupGeo &q = geo[static_cast<size_t>(g)];
-        std::memset(&q, 0, sizeof q);
-        q.first = static_cast<int32_t>(unit_group.size());
+        a_map.first_blk[g] = static_cast<int32_t>(a_nblk);
+        a_map.row0[g] = static_cast<int32_t>(offsets[g]);
+        GroupGeo &q = gp.g[g];
+        q.first = static_cast<int32_t>(units);
         q.bias_off = static_cast<int32_t>(g * N);
-        int64_t units_g;
         if (swap) {
             q.tiles_a = static_cast<int32_t>(cdiv(N, 128));
             q.oa = static_cast<int32_t>(g * N), q.sa = static_cast<int32_t>(g * nb), q.da = 0,
             q.la = static_cast<int32_t>(N);
-            q.ob = static_cast<int32_t>(offsets[g]), q.sb = static_cast<int32_t>(blk0),
+            q.ob = static_cast<int32_t>(offsets[g]), q.sb = static_cast<int32_t>(a_nblk),
             q.db = static_cast<int32_t>(offsets[g]), q.lb = static_cast<int32_t>(m);
-            units_g = q.tiles_a * cdiv(m, bn);
+            units += q.tiles_a * cdiv(m, bn);
         } else {
             q.tiles_a = static_cast<int32_t>(cdiv(m, 128 * cg));
-            q.oa = static_cast<int32_t>(offsets[g]), q.sa = static_cast<int32_t>(blk0),
+            q.oa = static_cast<int32_t>(offsets[g]), q.sa = static_cast<int32_t>(a_nblk),
             q.da = static_cast<int32_t>(offsets[g]), q.la = static_cast<int32_t>(m);
             q.ob = static_cast<int32_t>(g * N), q.sb = static_cast<int32_t>(g * nb), q.db = 0,
             q.lb = static_cast<int32_t>(N);
-            units_g = q.tiles_a * cdiv(N, bn);
+            units += q.tiles_a * cdiv(N, bn);
         }
-        unit_group.insert(unit_group.end(), static_cast<size_t>(units_g), static_cast<int32_t>(g));
+        if (q.tiles_a == 0) q.tiles_a = 1;        // (an empty group owns no unit)
+        a_nblk += cdiv(m, 128);
     }
-    if (!b_pre)
-        for (int64_t g = 0; g < G; ++g)
-            for (int64_t b = 0; b < nb; ++b)
-                b_blocks.push_back(make_int2(static_cast<int>(g * N + 128 * b),
-                                             static_cast<int>(std::min<int64_t>(128, N - 128 * b))));
-    const int64_t units = static_cast<int64_t>(unit_group.size());
+    a_map.first_blk[G] = static_cast<int32_t>(a_nblk);
+    a_map.row0[G] = static_cast<int32_t>(M);
     if (units > (1ll << 30)) return FP4_ERR_UNSUPPORTED;
+    RowBlocks b_map;
+    std::memset(&b_map, 0, sizeof b_map);
+    b_map.groups = static_cast<int32_t>(G);
+    b_map.uniform = static_cast<int32_t>(N);
 
-    // scratch: [A atoms][B atoms][tables], each 256-byte aligned
+    // scratch (stream-ordered): the reordered scales, 256-byte aligned
     auto up = [](size_t b) { return (b + 255) & ~static_cast<size_t>(255); };
-    const int64_t a_nblk = static_cast<int64_t>(a_blocks.size());
     const size_t atoms_a = a_pre ? 0 : static_cast<size_t>(a_nblk * kc4 * kAtomBytes);
     const size_t atoms_b = b_pre ? 0 : static_cast<size_t>(G * nb * kc4 * kAtomBytes);
-    const size_t t_ablk = a_blocks.size() * sizeof(int2), t_bblk = b_blocks.size() * sizeof(int2);
-    const size_t t_units = unit_group.size() * sizeof(int32_t), t_geo = geo.size() * sizeof(GroupGeo);
-    const size_t off_b = up(atoms_a), off_tab = off_b + up(atoms_b);
-    const size_t off_bblk = up(t_ablk), off_units = off_bblk + up(t_bblk), off_geo = off_units + up(t_units);
-    const size_t tab_bytes = off_geo + up(t_geo);
-    std::vector<uint8_t> host_tab(tab_bytes, 0);
-    std::memcpy(host_tab.data(), a_blocks.data(), t_ablk);
-    if (t_bblk) std::memcpy(host_tab.data() + off_bblk, b_blocks.data(), t_bblk);
-    std::memcpy(host_tab.data() + off_units, unit_group.data(), t_units);
-    std::memcpy(host_tab.data() + off_geo, geo.data(), t_geo);
+    const size_t off_b = up(atoms_a);
     uint8_t *scratch = nullptr;
-    if (cudaMallocAsync(reinterpret_cast<void **>(&scratch), off_tab + tab_bytes, stream) != cudaSuccess)
+    if (atoms_a + atoms_b > 0 &&
+        cudaMallocAsync(reinterpret_cast<void **>(&scratch), off_b + atoms_b, stream) != cudaSuccess)
         return FP4_ERR_CUDA;
     fp4_status result = FP4_OK;
     do {
-        uint8_t *tab = scratch + off_tab;
-        // pageable source: the call returns once the bytes are staged, so the
-        // host vector may go out of scope
-        if (cudaMemcpyAsync(tab, host_tab.data(), tab_bytes, cudaMemcpyHostToDevice, stream) != cudaSuccess) {
-            result = FP4_ERR_CUDA;
-            break;
-        }
         const uint8_t *a_atoms = static_cast<const uint8_t *>(sfA);
         const uint8_t *b_atoms = static_cast<const uint8_t *>(sfB);
         if (!a_pre) {
-            if ((result = reorder_launch(sfA, scratch, M, ksf, info->sms, stream, a_nblk,
-                                         reinterpret_cast<const int2 *>(tab))) != FP4_OK)
-                break;
+            if ((result = reorder_launch(sfA, scratch, M, ksf, info->sms, stream, a_nblk, &a_map)) != FP4_OK) break;
             a_atoms = scratch;
         }
         if (!b_pre) {
-            if ((result = reorder_launch(sfB, scratch + off_b, G * N, ksf, info->sms, stream, G * nb,
-                                         reinterpret_cast<const int2 *>(tab + off_bblk))) != FP4_OK)
+            if ((result = reorder_launch(sfB, scratch + off_b, G * N, ksf, info->sms, stream, G * nb, &b_map)) !=
+                FP4_OK)
                 break;
             b_atoms = scratch + off_b;
         }
@@ -1614,13 +1647,12 @@ fp4_status grouped_impl(fp4_format fmt, int prepacked, int64_t G, const int64_t 
         a.out = D;
         a.ldo = d_cols;
         a.split_units = 0;
-        a.unit_group = reinterpret_cast<const int32_t *>(tab + off_units);
-        a.geo = reinterpret_cast<const GroupGeo *>(tab + off_geo);
         a.epoch = ++g_epoch;
-        if (units > 0 && launch_grouped(cg, bn, mx, *info, static_cast<int>(units), m, a, stream) != cudaSuccess)
+        if (units > 0 &&
+            launch_grouped(cg, bn, mx, *info, static_cast<int>(units), m, a, gp, stream) != cudaSuccess)
             result = FP4_ERR_CUDA;
     } while (false);
-    if (cudaFreeAsync(scratch, stream) != cudaSuccess && result == FP4_OK) result = FP4_ERR_CUDA;
+    if (scratch && cudaFreeAsync(scratch, stream) != cudaSuccess && result == FP4_OK) result = FP4_ERR_CUDA;
     return result;
 }
 
@@ -1718,32 +1750,28 @@ fp4_status fp4_scale_reorder_grouped(const void *sf_plain, void *sf_atom, int64_
     if (k % vec != 0) return FP4_ERR_UNSUPPORTED;
     if (G == 0 || k == 0) return FP4_OK;
     if (!offsets || offsets[0] != 0) return FP4_ERR_INVALID_ARG;
-    std::vector<int2> blocks;
+    if (G > kMaxGroups) return FP4_ERR_UNSUPPORTED;
+    RowBlocks map;
+    std::memset(&map, 0, sizeof map);
+    map.groups = static_cast<int32_t>(G);
+    int64_t blocks = 0;
     for (int64_t g = 0; g < G; ++g) {
-        const int64_t m = offsets[g + 1] - offsets[g];
-        if (m < 0) return FP4_ERR_INVALID_ARG;
-        for (int64_t b = 0; b < cdiv(m, 128); ++b)
-            blocks.push_back(make_int2(static_cast<int>(offsets[g] + 128 * b),
-                                       static_cast<int>(std::min<int64_t>(128, m - 128 * b))));
+        if (offsets[g + 1] < offsets[g]) return FP4_ERR_INVALID_ARG;
+        map.first_blk[g] = static_cast<int32_t>(blocks);
+        map.row0[g] = static_cast<int32_t>(offsets[g]);
+        blocks += cdiv(offsets[g + 1] - offsets[g], 128);
     }
     if (offsets[G] > (1ll << 30)) return FP4_ERR_UNSUPPORTED;
-    if (blocks.empty()) return FP4_OK;
+    map.first_blk[G] = static_cast<int32_t>(blocks);
+    map.row0[G] = static_cast<int32_t>(offsets[G]);
+    if (blocks == 0) return FP4_OK;
     if (!sf_plain || !sf_atom) return FP4_ERR_INVALID_ARG;
     if (!aligned16(sf_atom)) return FP4_ERR_MISALIGNED;
     int dev;
     DeviceInfo *info;
-    fp4_status st = device_info(dev, info);
+    const fp4_status st = device_info(dev, info);
     if (st != FP4_OK) return st;
-    const size_t bytes = blocks.size() * sizeof(int2);
-    int2 *table = nullptr;
-    if (cudaMallocAsync(reinterpret_cast<void **>(&table), bytes, stream) != cudaSuccess) return FP4_ERR_CUDA;
-    if (cudaMemcpyAsync(table, blocks.data(), bytes, cudaMemcpyHostToDevice, stream) != cudaSuccess)
-        st = FP4_ERR_CUDA;
-    if (st == FP4_OK)
-        st = reorder_launch(sf_plain, sf_atom, offsets[G], k / vec, info->sms, stream,
-                            static_cast<int64_t>(blocks.size()), table);
-    if (cudaFreeAsync(table, stream) != cudaSuccess && st == FP4_OK) st = FP4_ERR_CUDA;
-    return st;
+    return reorder_launch(sf_plain, sf_atom, offsets[G], k / vec, info->sms, stream, blocks, &map);
 }
 
 fp4_status fp4_gemm_fused(fp4_format fmt, int scales_prepacked, const void *A, const void *sfA, const void *B,

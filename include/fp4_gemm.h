@@ -198,13 +198,15 @@ fp4_status fp4_gemm_fused(fp4_format fmt, int scales_prepacked, const void *A, c
  *   epi      as fp4_gemm_fused; bias, if given, is [G][N] floats (per group).
  *   D        [M_total][N] (or [M_total][N/2] for SwiGLU).
  * One launch covers every group: the persistent kernel's tiles are the groups'
- * tiles back to back. Plan: swap-AB (weights on the MMA's M side, one tile of
- * a group's rows on its N side) when every group has at most 256 rows or D's
- * rows cannot take 16-byte stores, else direct; no K split. Scratch:
- * stream-ordered (the reordered scales and small per-group tables).
- * Requirements and errors as fp4_gemm; offsets not starting at 0 or
- * decreasing give FP4_ERR_INVALID_ARG; M_total or G * N above 2^30,
- * FP4_ERR_UNSUPPORTED. cfg may force mode 1 (direct) or 2 (swap-AB). */
+ * tiles back to back, the groups' geometry passed in its parameter block (no
+ * table upload, so the call never synchronises the host with the stream).
+ * Plan: swap-AB (weights on the MMA's M side, one tile of a group's rows on
+ * its N side) when every group has at most 256 rows or D's rows cannot take
+ * 16-byte stores, else direct; no K split. Scratch: stream-ordered (the
+ * reordered scales). Requirements and errors as fp4_gemm; offsets not
+ * starting at 0 or decreasing give FP4_ERR_INVALID_ARG; G above 256, M_total
+ * or G * N above 2^30, FP4_ERR_UNSUPPORTED. cfg may force mode 1 (direct) or
+ * 2 (swap-AB). */
 #define FP4_GROUPED_B_ATOMS 1   /* sfB: the G groups' atom-layout copies back to back */
 #define FP4_GROUPED_A_ATOMS 2   /* sfA: the grouped atom layout of fp4_scale_reorder_grouped */
 fp4_status fp4_gemm_grouped(fp4_format fmt, int scales_prepacked, int64_t G, const int64_t *offsets,
@@ -215,7 +217,8 @@ fp4_status fp4_gemm_grouped(fp4_format fmt, int scales_prepacked, int64_t G, con
 /* The grouped atom layout of activation scales: each group's rows
  * (offsets as fp4_gemm_grouped) reordered like fp4_scale_reorder, every group
  * starting a fresh 128-row block; fp4_scale_atom_bytes_grouped gives its size
- * (0 for invalid arguments). Host offsets; errors as fp4_scale_reorder. */
+ * (0 for invalid arguments). Host offsets, G <= 256; errors as
+ * fp4_scale_reorder. */
 size_t fp4_scale_atom_bytes_grouped(int64_t G, const int64_t *offsets, int64_t k, int vec);
 fp4_status fp4_scale_reorder_grouped(const void *sf_plain, void *sf_atom, int64_t G, const int64_t *offsets,
                                      int64_t k, int vec, cudaStream_t stream);

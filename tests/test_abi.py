@@ -160,6 +160,9 @@ def test_grouped_host_validation_without_device(fp4):
     assert grp([0, 4], cfg=ctypes.byref(fp4.GemmConfig(mode=5))) == 1
     assert grp([0, 4], cfg=ctypes.byref(fp4.GemmConfig(splits=2))) == 2
     assert lib.fp4_gemm_grouped(0, 0, 2, None, p, p, p, p, 1.0, None, p, 64, 64, 0, None, 0) == 1   # no offsets
+    assert grp(np.arange(258)) == 2                 # more than 256 groups
+    many = np.arange(258, dtype=np.int64)
+    assert lib.fp4_scale_reorder_grouped(p, p, 257, many.ctypes.data, 64, 16, 0) == 2
 
 
 def test_quantize_host_validation_without_device(fp4):
