@@ -21,7 +21,7 @@ __all__ = ["FP4_OK", "Fp4Error", "load", "build", "gemm", "gemm_nvfp4", "gemm_mx
            "gemm_mxfp4_prepacked", "gemm_host", "scale_reorder", "scale_atom_bytes", "get_device_status",
            "status_string", "set_wait_limit_ms", "GemmConfig", "FMT", "OUT", "gemm_static_scratch",
            "STATIC_SCRATCH_BYTES", "quantize", "IN", "SF_LAYOUT", "gemm_fused", "ACT", "Epilogue", "gemm_plan", "PlanInfo", "gemm_grouped", "scale_reorder_grouped",
-           "scale_atom_bytes_grouped"]
+           "scale_atom_bytes_grouped", "scale_reorder2"]
 
 FP4_OK = 0
 STATUS_NAMES = {0: "FP4_OK", 1: "FP4_ERR_INVALID_ARG", 2: "FP4_ERR_UNSUPPORTED", 3: "FP4_ERR_MISALIGNED",
@@ -101,6 +101,8 @@ def load():
     lib.fp4_scale_atom_bytes.restype = ctypes.c_size_t
     lib.fp4_scale_reorder.argtypes = [vp, vp, i64, i64, i32, vp]
     lib.fp4_scale_reorder.restype = i32
+    lib.fp4_scale_reorder2.argtypes = [vp, vp, i64, vp, vp, i64, i64, i32, vp]
+    lib.fp4_scale_reorder2.restype = i32
     lib.fp4_get_device_status.argtypes = [vp]
     lib.fp4_get_device_status.restype = i32
     lib.fp4_status_string.argtypes = [i32]
@@ -171,6 +173,16 @@ def gemm_fused(fmt: str, A, sfA, B, sfB, alpha: float, D, M: int, N: int, K: int
 def _offsets(offsets):
     import numpy as np
     return np.ascontiguousarray(np.asarray(offsets, dtype=np.int64))
+
+
+def scale_reorder2(sf_a, atoms_a, rows_a: int, sf_b, atoms_b, rows_b: int, K: int, vec: int, stream=None,
+                   check: bool = True) -> int:
+    """fp4_scale_reorder2: both operands' scales in one launch."""
+    st = load().fp4_scale_reorder2(_ptr(sf_a), _ptr(atoms_a), int(rows_a), _ptr(sf_b), _ptr(atoms_b), int(rows_b),
+                                   int(K), int(vec), _stream(stream))
+    if check:
+        _check(st, "fp4_scale_reorder2")
+    return st
 
 
 def scale_atom_bytes_grouped(offsets, K: int, vec: int) -> int:

@@ -858,11 +858,6 @@ __global__ void splitk_reduce_kernel(const float *__restrict__ ws, void *__restr
     }
 }
 
-// Scale reorder: row-major sf[rows][ksf] -> 128x4 atoms. One thread writes one
-// 16-byte line of an atom: line i of atom (rb, cb) holds rows rb*128 + i + 32j
-// (j = 0..3), columns 4cb..4cb+3 (zero past the matrix). A block of 256 threads
-// covers 8 consecutive atoms of one 128-row block, so its reads of a row fall
-// in one or two 32-byte sectors.
 // Which source rows an atom row-block holds. Plain (groups == 0): block rb
 // holds rows rb*128 .. of a `rows`-row matrix. Grouped (each group's rows start
 // a fresh 128-row block): every group `uniform` rows (uniform > 0), or group g
@@ -874,51 +869,90 @@ struct RowBlocks {
     int32_t row0[kMaxGroups + 1];
 };
 
-__global__ void scale_reorder_kernel(const uint8_t *__restrict__ sf, uint4 *__restrict__ out, int64_t rows,
-                                     int64_t ksf, int64_t kc4, int64_t lines, const __grid_constant__ RowBlocks rbm)
+__device__ __forceinline__ void block_rows(const RowBlocks &rbm, int64_t rows, int64_t rb, int64_t &src0,
+                                           int64_t &valid)
 {
-    // 32-bit loads only when every row's 4-column group is 4-byte aligned
-    const bool words = (ksf & 3) == 0 && (reinterpret_cast<uintptr_t>(sf) & 3) == 0;
-    for (int64_t l = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; l < lines;
-         l += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        const int64_t atom = l >> 5;
-        const int i = static_cast<int>(l & 31);
-        const int64_t rb = atom / kc4, cb = atom - rb * kc4;
-        const int64_t c0 = cb * 4;
-        int64_t src0 = rb * 128, valid = rows - rb * 128;
-        if (rbm.groups > 0 && rbm.uniform > 0) {
-            const int64_t per = (rbm.uniform + 127) / 128;
-            const int64_t g = rb / per, b = rb - g * per;
-            src0 = g * rbm.uniform + 128 * b;
-            valid = rbm.uniform - 128 * b;
-        } else if (rbm.groups > 0) {
-            int lo = 0, hi = rbm.groups - 1;          // the last group starting at or before rb
-            while (lo < hi) {
-                const int mid = (lo + hi + 1) >> 1;
-                if (rbm.first_blk[mid] <= rb) lo = mid; else hi = mid - 1;
-            }
-            const int64_t b = rb - rbm.first_blk[lo];
-            src0 = rbm.row0[lo] + 128 * b;
-            valid = rbm.row0[lo + 1] - rbm.row0[lo] - 128 * b;
+    src0 = rb * 128;
+    valid = rows - rb * 128;
+    if (rbm.groups > 0 && rbm.uniform > 0) {
+        const int64_t per = (rbm.uniform + 127) / 128;
+        const int64_t g = rb / per, b = rb - g * per;
+        src0 = g * rbm.uniform + 128 * b;
+        valid = rbm.uniform - 128 * b;
+    } else if (rbm.groups > 0) {
+        int lo = 0, hi = rbm.groups - 1;          // the last group starting at or before rb
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (rbm.first_blk[mid] <= rb) lo = mid; else hi = mid - 1;
         }
-        uint32_t w[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int64_t r = src0 + 32 * j + i;
-            uint32_t word = 0;
-            if (32 * j + i < valid) {
-                const uint8_t *row = sf + r * ksf;
-                if (words) {
-                    word = __ldg(reinterpret_cast<const uint32_t *>(row + c0));
+        const int64_t b = rb - rbm.first_blk[lo];
+        src0 = rbm.row0[lo] + 128 * b;
+        valid = rbm.row0[lo + 1] - rbm.row0[lo] - 128 * b;
+    }
+    valid = valid < 0 ? 0 : (valid > 128 ? 128 : valid);
+}
+
+// Scale reorder: row-major sf[rows][ksf] -> 128x4 atoms. A CTA takes a tile of
+// one 128-row block x 32 scale columns (8 atoms): each thread reads one
+// 16-byte piece (two per row, so a warp's load covers whole 32-byte sectors of
+// 16 rows) into shared memory (rows padded to 9 words, so the transposing
+// reads below are conflict-free), then writes one 16-byte atom line -- line i
+// of an atom holds rows i, i+32, i+64, i+96 of the block, 4 columns each -- so
+// a warp writes one 512-byte atom. Zero past the matrix. One launch can carry
+// two matrices (the two operands of a GEMM call): job 0's tiles, then job 1's.
+constexpr int kReorderThreads = 256;
+constexpr int kReorderAtoms = 8;                  // atoms (of 4 scale columns) per tile
+constexpr int kReorderRowWords = kReorderAtoms + 1;
+
+struct ReorderJob {
+    const uint8_t *sf;
+    uint4 *out;
+    int64_t rows, row_blocks, tiles;
+};
+
+__global__ void __launch_bounds__(kReorderThreads)
+    scale_reorder_kernel(ReorderJob j0, ReorderJob j1, int64_t ksf, int64_t kc4,
+                         const __grid_constant__ RowBlocks map0, const __grid_constant__ RowBlocks map1)
+{
+    __shared__ uint32_t tile[128 * kReorderRowWords];
+    const int64_t col_tiles = (kc4 + kReorderAtoms - 1) / kReorderAtoms;
+    const int64_t ncols = kReorderAtoms * 4;
+    for (int64_t t = blockIdx.x; t < j0.tiles + j1.tiles; t += gridDim.x) {
+        const bool second = t >= j0.tiles;
+        const ReorderJob &j = second ? j1 : j0;
+        const int64_t tt = second ? t - j0.tiles : t;
+        const int64_t rb = tt / col_tiles, ct = tt - rb * col_tiles;
+        int64_t src0, valid;
+        block_rows(second ? map1 : map0, j.rows, rb, src0, valid);
+        const int64_t c0 = ct * ncols;                // first scale column of the tile
+        const bool vec16 = (ksf & 15) == 0 && (reinterpret_cast<uintptr_t>(j.sf) & 15) == 0;
+        __syncthreads();                              // the previous tile's reads are done
+        {
+            const int r = threadIdx.x >> 1, pc = threadIdx.x & 1;   // row, 16-byte piece
+            const int64_t col = c0 + 16 * pc;
+            uint32_t w[4] = {0u, 0u, 0u, 0u};
+            if (r < valid && col < ksf) {
+                const uint8_t *src = j.sf + (src0 + r) * ksf + col;
+                if (vec16) {
+                    const uint4 v = __ldg(reinterpret_cast<const uint4 *>(src));
+                    w[0] = v.x, w[1] = v.y, w[2] = v.z, w[3] = v.w;
                 } else {
-#pragma unroll
-                    for (int t = 0; t < 4; ++t)
-                        if (c0 + t < ksf) word |= static_cast<uint32_t>(__ldg(row + c0 + t)) << (8 * t);
+                    for (int b = 0; b < 16 && col + b < ksf; ++b)
+                        w[b >> 2] |= static_cast<uint32_t>(__ldg(src + b)) << (8 * (b & 3));
                 }
             }
-            w[j] = word;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) tile[r * kReorderRowWords + 4 * pc + q] = w[q];
         }
-        out[l] = make_uint4(w[0], w[1], w[2], w[3]);
+        __syncthreads();
+        {
+            const int a = threadIdx.x >> 5, i = threadIdx.x & 31;  // line i of atom a
+            if (ct * kReorderAtoms + a < kc4) {
+                const uint4 v = make_uint4(tile[i * kReorderRowWords + a], tile[(i + 32) * kReorderRowWords + a],
+                                           tile[(i + 64) * kReorderRowWords + a], tile[(i + 96) * kReorderRowWords + a]);
+                j.out[(rb * kc4 + ct * kReorderAtoms + a) * 32 + i] = v;
+            }
+        }
     }
 }
 
@@ -1253,20 +1287,50 @@ fp4_status make_plan(int64_t M, int64_t N, int64_t K, bool rows_ok, bool mx, int
     return FP4_OK;
 }
 
-// `row_blocks` / `rbm`: the grouped forms (see RowBlocks).
+// One reorder launch for up to two scale matrices with the same K (the second
+// may be absent: sf1 == nullptr). `row_blocks` / `rbm`: the grouped forms (see
+// RowBlocks); plain when rbm is null.
+struct ReorderSpec {
+    const void *sf = nullptr;
+    void *out = nullptr;
+    int64_t rows = 0;
+    int64_t row_blocks = -1;
+    const RowBlocks *rbm = nullptr;
+};
+
+fp4_status reorder2_launch(const ReorderSpec &a, const ReorderSpec &b, int64_t ksf, int sms, cudaStream_t stream)
+{
+    const int64_t kc4 = cdiv(ksf, 4);
+    const int64_t col_tiles = cdiv(kc4, kReorderAtoms);
+    auto job = [&](const ReorderSpec &sp) {
+        ReorderJob j;
+        j.sf = static_cast<const uint8_t *>(sp.sf);
+        j.out = static_cast<uint4 *>(sp.out);
+        j.rows = sp.rows;
+        j.row_blocks = sp.sf ? (sp.rbm ? sp.row_blocks : cdiv(sp.rows, 128)) : 0;
+        j.tiles = j.row_blocks * col_tiles;
+        return j;
+    };
+    const ReorderJob j0 = job(a), j1 = job(b);
+    const int64_t tiles = j0.tiles + j1.tiles;
+    if (tiles == 0) return FP4_OK;
+    const int64_t blocks = std::min<int64_t>(tiles, static_cast<int64_t>(sms) * 8);
+    static const RowBlocks plain = {};
+    scale_reorder_kernel<<<static_cast<unsigned>(blocks), kReorderThreads, 0, stream>>>(
+        j0, j1, ksf, kc4, a.rbm ? *a.rbm : plain, b.rbm ? *b.rbm : plain);
+    return cudaGetLastError() == cudaSuccess ? FP4_OK : FP4_ERR_CUDA;
+}
+
 fp4_status reorder_launch(const void *sf_plain, void *sf_atom, int64_t rows, int64_t ksf, int sms,
                           cudaStream_t stream, int64_t row_blocks = -1, const RowBlocks *rbm = nullptr)
 {
-    const int64_t kc4 = cdiv(ksf, 4);
-    const int64_t lines = (rbm ? row_blocks : cdiv(rows, 128)) * kc4 * 32;
-    if (lines == 0) return FP4_OK;
-    const int threads = 256;
-    const int64_t blocks = std::min<int64_t>(cdiv(lines, threads), static_cast<int64_t>(sms) * 32);
-    static const RowBlocks plain = {};
-    scale_reorder_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
-        static_cast<const uint8_t *>(sf_plain), static_cast<uint4 *>(sf_atom), rows, ksf, kc4, lines,
-        rbm ? *rbm : plain);
-    return cudaGetLastError() == cudaSuccess ? FP4_OK : FP4_ERR_CUDA;
+    ReorderSpec a;
+    a.sf = sf_plain;
+    a.out = sf_atom;
+    a.rows = rows;
+    a.row_blocks = row_blocks;
+    a.rbm = rbm;
+    return reorder2_launch(a, ReorderSpec(), ksf, sms, stream);
 }
 
 // `ext_scratch` (with `ext_bytes`), when given, replaces the stream-ordered
@@ -1398,8 +1462,10 @@ fp4_status gemm_impl(fp4_format fmt, int prepacked, const void *A, const void *s
         const uint8_t *sfb_atoms = static_cast<const uint8_t *>(sf_b);
         uint8_t *ws = scratch + (prepacked ? 0 : atoms_a + atoms_b);
         if (!prepacked) {
-            if ((result = reorder_launch(sf_a, scratch, rows_a, ksf, info->sms, stream)) != FP4_OK) break;
-            if ((result = reorder_launch(sf_b, scratch + atoms_a, rows_b, ksf, info->sms, stream)) != FP4_OK) break;
+            ReorderSpec ra, rbs;
+            ra.sf = sf_a, ra.out = scratch, ra.rows = rows_a;
+            rbs.sf = sf_b, rbs.out = scratch + atoms_a, rbs.rows = rows_b;
+            if ((result = reorder2_launch(ra, rbs, ksf, info->sms, stream)) != FP4_OK) break;
             sfa_atoms = scratch;
             sfb_atoms = scratch + atoms_a;
         }
@@ -1605,15 +1671,17 @@ fp4_status grouped_impl(fp4_format fmt, int prepacked, int64_t G, const int64_t 
     do {
         const uint8_t *a_atoms = static_cast<const uint8_t *>(sfA);
         const uint8_t *b_atoms = static_cast<const uint8_t *>(sfB);
-        if (!a_pre) {
-            if ((result = reorder_launch(sfA, scratch, M, ksf, info->sms, stream, a_nblk, &a_map)) != FP4_OK) break;
-            a_atoms = scratch;
-        }
-        if (!b_pre) {
-            if ((result = reorder_launch(sfB, scratch + off_b, G * N, ksf, info->sms, stream, G * nb, &b_map)) !=
-                FP4_OK)
-                break;
-            b_atoms = scratch + off_b;
+        {
+            ReorderSpec ra, rbs;                      // both in one launch
+            if (!a_pre) {
+                ra.sf = sfA, ra.out = scratch, ra.rows = M, ra.row_blocks = a_nblk, ra.rbm = &a_map;
+                a_atoms = scratch;
+            }
+            if (!b_pre) {
+                rbs.sf = sfB, rbs.out = scratch + off_b, rbs.rows = G * N, rbs.row_blocks = G * nb, rbs.rbm = &b_map;
+                b_atoms = scratch + off_b;
+            }
+            if ((result = reorder2_launch(ra, rbs, ksf, info->sms, stream)) != FP4_OK) break;
         }
         const int apk = mx ? 2 : 4;
         Maps m;
@@ -1720,7 +1788,7 @@ fp4_status fp4_gemm_plan(fp4_format fmt, int scales_prepacked, int64_t M, int64_
     info->bn = plan.bn;
     info->cta_group = plan.cg;
     info->splits = static_cast<int32_t>(cdiv(cdiv(K, kBK), cdiv(cdiv(K, kBK), plan.splits)));
-    info->launches = (scales_prepacked ? 0 : 2) + 1 + (info->splits > 1 ? 1 : 0);
+    info->launches = (scales_prepacked ? 0 : 1) + 1 + (info->splits > 1 ? 1 : 0);
     return FP4_OK;
 }
 
@@ -1870,6 +1938,24 @@ fp4_status fp4_scale_reorder(const void *sf_plain, void *sf_atom, int64_t rows, 
     fp4_status st = device_info(dev, info);
     if (st != FP4_OK) return st;
     return reorder_launch(sf_plain, sf_atom, rows, k / vec, info->sms, stream);
+}
+
+fp4_status fp4_scale_reorder2(const void *sf_a, void *atoms_a, int64_t rows_a, const void *sf_b, void *atoms_b,
+                              int64_t rows_b, int64_t k, int vec, cudaStream_t stream)
+{
+    if (rows_a < 0 || rows_b < 0 || k < 0 || (vec != 16 && vec != 32)) return FP4_ERR_INVALID_ARG;
+    if (k % vec != 0) return FP4_ERR_UNSUPPORTED;
+    if (k == 0 || (rows_a == 0 && rows_b == 0)) return FP4_OK;
+    if ((rows_a && (!sf_a || !atoms_a)) || (rows_b && (!sf_b || !atoms_b))) return FP4_ERR_INVALID_ARG;
+    if ((rows_a && !aligned16(atoms_a)) || (rows_b && !aligned16(atoms_b))) return FP4_ERR_MISALIGNED;
+    int dev;
+    DeviceInfo *info;
+    const fp4_status st = device_info(dev, info);
+    if (st != FP4_OK) return st;
+    ReorderSpec a, b;
+    if (rows_a) a.sf = sf_a, a.out = atoms_a, a.rows = rows_a;
+    if (rows_b) b.sf = sf_b, b.out = atoms_b, b.rows = rows_b;
+    return reorder2_launch(a, b, k / vec, info->sms, stream);
 }
 
 fp4_status fp4_get_device_status(cudaStream_t stream)

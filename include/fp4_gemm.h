@@ -268,6 +268,13 @@ size_t fp4_scale_atom_bytes(int64_t rows, int64_t k, int vec);
 fp4_status fp4_scale_reorder(const void *sf_plain, void *sf_atom, int64_t rows, int64_t k,
                              int vec, cudaStream_t stream);
 
+/* Both operands' scales of one GEMM in one launch (what the plain-scale calls
+ * launch before the GEMM): sf_a -> atoms_a (rows_a rows), sf_b -> atoms_b
+ * (rows_b rows), same k and vec; a side with 0 rows is skipped. As
+ * fp4_scale_reorder otherwise. */
+fp4_status fp4_scale_reorder2(const void *sf_a, void *atoms_a, int64_t rows_a, const void *sf_b, void *atoms_b,
+                              int64_t rows_b, int64_t k, int vec, cudaStream_t stream);
+
 /* Synchronises `stream`, then returns and clears the current device's status
  * word (FP4_OK, or FP4_ERR_TIMEOUT if a bounded wait ran out since the last call). */
 fp4_status fp4_get_device_status(cudaStream_t stream);

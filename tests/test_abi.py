@@ -96,6 +96,11 @@ def test_host_validation_without_device(fp4):
     assert lib.fp4_scale_reorder(p, p + 4, 10, 64, 16, 0) == 3
     assert lib.fp4_scale_reorder(p, p, 0, 64, 16, 0) == 0
     assert lib.fp4_gemm_host(0, p, p, p, p, 1.0, p, 64, 64, 40, 0, 0) == 2
+    assert lib.fp4_scale_reorder2(p, p, 10, p, p, 10, 48, 32, 0) == 2
+    assert lib.fp4_scale_reorder2(p, p, -1, p, p, 10, 64, 16, 0) == 1
+    assert lib.fp4_scale_reorder2(None, p, 10, p, p, 10, 64, 16, 0) == 1
+    assert lib.fp4_scale_reorder2(p, p, 10, p, p + 4, 10, 64, 16, 0) == 3
+    assert lib.fp4_scale_reorder2(p, p, 0, p, p, 0, 64, 16, 0) == 0
 
 
 def test_fused_host_validation_without_device(fp4):

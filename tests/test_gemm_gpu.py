@@ -111,6 +111,23 @@ def check_sampled(orc, inp, got, seed=0, n_random=8, n_pairs=4000):
 
 # ---- scale reorder ------------------------------------------------------------------
 
+@pytest.mark.parametrize("ra,rb,K,vec", [(300, 1000, 288, 16), (1, 129, 4096, 16), (0, 77, 96, 32), (64, 0, 64, 32)])
+def test_scale_reorder2_bit_exact(fp4, orc, ra, rb, K, vec):
+    # both operands in one launch: each equal to the oracle's reorder
+    rng = np.random.default_rng(ra + rb + K)
+    sa = rng.integers(0, 256, (ra, K // vec)).astype(np.uint8)
+    sb = rng.integers(0, 256, (rb, K // vec)).astype(np.uint8)
+    na, nb = fp4.scale_atom_bytes(ra, K, vec), fp4.scale_atom_bytes(rb, K, vec)
+    oa = torch.full((max(na, 16),), 0xCD, dtype=torch.uint8, device="cuda")
+    ob = torch.full((max(nb, 16),), 0xCD, dtype=torch.uint8, device="cuda")
+    fp4.scale_reorder2(_dev(sa) if ra else None, oa, ra, _dev(sb) if rb else None, ob, rb, K, vec)
+    torch.cuda.synchronize()
+    if ra:
+        np.testing.assert_array_equal(oa.cpu().numpy()[:na], orc.scale_reorder(sa, ra, K // vec))
+    if rb:
+        np.testing.assert_array_equal(ob.cpu().numpy()[:nb], orc.scale_reorder(sb, rb, K // vec))
+
+
 @pytest.mark.parametrize("rows,K,vec", [(128, 64, 16), (300, 288, 16), (1, 32, 32), (257, 4096, 16),
                                         (1000, 96, 32), (14336, 4096, 16), (129, 5120, 32)])
 def test_scale_reorder_bit_exact(fp4, orc, rows, K, vec):
