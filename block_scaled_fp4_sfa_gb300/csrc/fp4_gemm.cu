@@ -462,6 +462,9 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tmap_a, const CUten
     if constexpr (CG == 2) cluster_sync(); else __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
+    // Launched as a dependent of the scale reorder, the set-up above overlaps
+    // its tail; nothing in memory is touched before it has completed.
+    griddep_wait();
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
@@ -915,6 +918,7 @@ __global__ void __launch_bounds__(kReorderThreads)
                          const __grid_constant__ RowBlocks map0, const __grid_constant__ RowBlocks map1)
 {
     __shared__ uint32_t tile[128 * kReorderRowWords];
+    griddep_launch_dependents();          // the GEMM that follows may start its set-up
     const int64_t col_tiles = (kc4 + kReorderAtoms - 1) / kReorderAtoms;
     const int64_t ncols = kReorderAtoms * 4;
     for (int64_t t = blockIdx.x; t < j0.tiles + j1.tiles; t += gridDim.x) {
@@ -1073,11 +1077,13 @@ cudaError_t launch_gemm(DeviceInfo &info, int kidx, int units, int cap, const Ma
         if constexpr (GROUPED) return fp4_gemm_grouped_kernel<CG, BN, MX>;
         else return fp4_gemm_kernel<CG, BN, MX>;
     }();
-    cudaLaunchAttribute cluster_attr[1];
+    cudaLaunchAttribute cluster_attr[2];
     cluster_attr[0].id = cudaLaunchAttributeClusterDimension;
     cluster_attr[0].val.clusterDim.x = CG;
     cluster_attr[0].val.clusterDim.y = 1;
     cluster_attr[0].val.clusterDim.z = 1;
+    cluster_attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    cluster_attr[1].val.programmaticStreamSerializationAllowed = 1;
     if (!info.attr_set[kidx]) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
         if (e != cudaSuccess) return e;
@@ -1112,10 +1118,10 @@ cudaError_t launch_gemm(DeviceInfo &info, int kidx, int units, int cap, const Ma
     lc.blockDim = dim3(kThreads, 1, 1);
     lc.dynamicSmemBytes = C::SMEM_BYTES;
     lc.stream = stream;
-    if (CG == 2) {
-        lc.attrs = cluster_attr;
-        lc.numAttrs = 1;
-    }
+    // a pair needs its cluster shape; every launch may start as a programmatic
+    // dependent of the preceding kernel (see griddep_wait)
+    lc.attrs = CG == 2 ? cluster_attr : cluster_attr + 1;
+    lc.numAttrs = CG == 2 ? 2 : 1;
     if constexpr (GROUPED)
         return cudaLaunchKernelEx(&lc, kern, m.a, m.b, m.sfa, m.sfb, args, *gp);
     else

@@ -362,3 +362,9 @@ __host__ __device__ constexpr uint32_t idesc_fp4(uint32_t m, uint32_t n, bool ue
 }
 
 }  // namespace fp4
+
+// Programmatic dependent launch: wait until the preceding grid in the stream
+// has completed and its writes are visible (a no-op when this grid was not
+// launched as a dependent), and let the next grid start its prologue early.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
