@@ -157,6 +157,7 @@ struct Cfg {
     static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
     static constexpr int SLOTS = STAGES;
     static constexpr int ACC_BUFS = BN <= 128 ? 2 : 1;
+    static constexpr bool WAITER_COPIES = CG == 1 && !MX;   // who issues the scale copies (see the waiter warp)
     static constexpr int SF_COLS = 4 * APK * (1 + NRB);        // TMEM columns of one k-tile's scales
     static constexpr int SF_TMEM = ACC_BUFS * BN;               // first scale column
     static constexpr int TMEM_USED = ACC_BUFS * BN + SLOTS * SF_COLS;
@@ -174,6 +175,7 @@ struct Cfg {
     static_assert(CG == 1 || CG == 2, "CTA group of 1 or 2");
     static_assert(CG == 1 || BN >= 128, "paired CTAs use N tiles of 128 or 256");
     static_assert(STAGES >= 2, "too few pipeline stages");
+    static_assert(24 * STAGES + 56 <= BAR_BYTES, "barriers, flags and the scale-copy barriers fit");
     static_assert(TMEM_USED <= 512, "TMEM budget exceeded");
     static_assert(SMEM_BYTES <= kSmemLimit, "shared memory budget exceeded");
     static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N must be a multiple of 16 in [16, 256]");
@@ -427,6 +429,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tmap_a, const CUten
         reinterpret_cast<volatile uint32_t *>(base_ptr + C::OFF_BAR + 16 * C::STAGES + 44);
     // stages the waiter warp has seen land (a count, in the MMA issue order)
     const uint32_t ready_addr = base + C::OFF_BAR + 16 * C::STAGES + 48;
+    const uint32_t bar_sf = base + C::OFF_BAR + 16 * C::STAGES + 56;     // scale copies of stage s done
 
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
@@ -444,6 +447,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tmap_a, const CUten
             mbar_init(bar_acc_empty + 8 * b, kEpiWarps * CG);
         }
         mbar_init(bar_drain, 1);
+        for (int st = 0; st < C::STAGES; ++st) mbar_init(bar_sf + 8 * st, 1);
         *abort_flag = 0;
         st_release_shared(ready_addr, 0);
         fence_mbarrier_init();
@@ -525,7 +529,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tmap_a, const CUten
             // apart; MMA j of a k-tile starts 32 bytes (two 16-byte units) in.
             const uint64_t desc_a0 = smem_desc(base + C::OFF_A, 16, 1024, 2);
             const uint64_t desc_b0 = smem_desc(base + C::OFF_B, 16, 1024, 2);
-            // A scale atom: 32 rows of 16 bytes, 8-row groups 128 bytes apart.
+            // scale atom: 32 rows of 16 bytes, 8-row groups 128 bytes apart
             const uint64_t desc_sfa0 = smem_desc(base + C::OFF_SFA, 0, 128, 0);
             const uint64_t desc_sfb0 = smem_desc(base + C::OFF_SFB, 0, 128, 0);
             int stage = 0;
@@ -552,15 +556,17 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tmap_a, const CUten
                     {
                         const int slot = stage;
                         const uint32_t sf = tmem + static_cast<uint32_t>(C::SF_TMEM + slot * C::SF_COLS);
-                        const uint64_t dsa = desc_sfa0 + static_cast<uint64_t>((slot * C::SFA_BYTES) >> 4);
-                        const uint64_t dsb = desc_sfb0 + static_cast<uint64_t>((slot * C::SFB_BYTES) >> 4);
+                        if constexpr (!C::WAITER_COPIES) {
+                            const uint64_t dsa = desc_sfa0 + static_cast<uint64_t>((slot * C::SFA_BYTES) >> 4);
+                            const uint64_t dsb = desc_sfb0 + static_cast<uint64_t>((slot * C::SFB_BYTES) >> 4);
 #pragma unroll
-                        for (int t = 0; t < C::APK; ++t) {
-                            tc_cp_32x128b_warpx4<CG>(sf + 4 * t, dsa + (t * kAtomBytes >> 4));
+                            for (int t = 0; t < C::APK; ++t) {
+                                tc_cp_32x128b_warpx4<CG>(sf + 4 * t, dsa + (t * kAtomBytes >> 4));
 #pragma unroll
-                            for (int rb = 0; rb < C::NRB; ++rb)
-                                tc_cp_32x128b_warpx4<CG>(sf + 4 * C::APK + 4 * (t * C::NRB + rb),
-                                                         dsb + ((rb * C::APK + t) * kAtomBytes >> 4));
+                                for (int rb = 0; rb < C::NRB; ++rb)
+                                    tc_cp_32x128b_warpx4<CG>(sf + 4 * C::APK + 4 * (t * C::NRB + rb),
+                                                             dsb + ((rb * C::APK + t) * kAtomBytes >> 4));
+                            }
                         }
                         const uint64_t da = desc_a0 + static_cast<uint64_t>((slot * C::A_BYTES) >> 4);
                         const uint64_t db = desc_b0 + static_cast<uint64_t>((slot * C::B_BYTES) >> 4);
@@ -594,8 +600,19 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tmap_a, const CUten
         // Waits, in the MMA issue order, for each stage to land and publishes
         // the running count, so that the MMA thread blocks in an mbarrier wait
         // only once per tile (for the accumulator): on this part a wait in the
-        // issuing thread costs about 200 cycles in which the tensor core runs dry.
+        // issuing thread costs about 200 cycles in which the tensor core runs
+        // dry. For NVFP4 with one CTA per MMA (twelve scale copies per k-tile)
+        // it also copies the stage's scale atoms into the stage's TMEM slot
+        // (tcgen05.cp) and waits for them before publishing, so that the copies
+        // overlap the MMAs of earlier stages instead of queueing behind them in
+        // the MMA thread (4096^3 55.4 -> 51.4 us, 8192 x 4096 x 14336
+        // 262 -> 236 us). MXFP4 (six copies per k-tile) keeps them in the MMA
+        // thread: there the split measured slower (8192^3 with CTA pairs
+        // 231 -> 287 us, with one CTA per MMA 250 -> 274 us).
         if (lane == 0 && rank == 0) {
+            // scale atom: 32 rows of 16 bytes, 8-row groups 128 bytes apart
+            const uint64_t desc_sfa0 = smem_desc(base + C::OFF_SFA, 0, 128, 0);
+            const uint64_t desc_sfb0 = smem_desc(base + C::OFF_SFB, 0, 128, 0);
             int stage = 0;
             uint32_t phase = 0;
             uint32_t seen = 0;
@@ -607,6 +624,26 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tmap_a, const CUten
                     if (!wait(bar_full + 8 * stage, phase, args.wait_ns, abort_flag)) {
                         ok = false;
                         break;
+                    }
+                    if constexpr (C::WAITER_COPIES) {
+                        tc_fence_after();
+                        const uint32_t sf = tmem + static_cast<uint32_t>(C::SF_TMEM + stage * C::SF_COLS);
+                        const uint64_t dsa = desc_sfa0 + static_cast<uint64_t>((stage * C::SFA_BYTES) >> 4);
+                        const uint64_t dsb = desc_sfb0 + static_cast<uint64_t>((stage * C::SFB_BYTES) >> 4);
+#pragma unroll
+                        for (int t = 0; t < C::APK; ++t) {
+                            tc_cp_32x128b_warpx4<CG>(sf + 4 * t, dsa + (t * kAtomBytes >> 4));
+#pragma unroll
+                            for (int rb = 0; rb < C::NRB; ++rb)
+                                tc_cp_32x128b_warpx4<CG>(sf + 4 * C::APK + 4 * (t * C::NRB + rb),
+                                                         dsb + ((rb * C::APK + t) * kAtomBytes >> 4));
+                        }
+                        tc_commit<CG>(bar_sf + 8 * stage, 1);     // this CTA's barrier only
+                        if (!wait(bar_sf + 8 * stage, phase, args.wait_ns, abort_flag)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_before();
                     }
                     st_release_shared(ready_addr, ++seen);
                     if (++stage == C::STAGES) {
