@@ -188,3 +188,16 @@ def test_grouped_workload_sampled(fp4, orc, name):
     ends = np.concatenate([gin.offsets[:-1][np.diff(gin.offsets) > 0], gin.offsets[1:][np.diff(gin.offsets) > 0] - 1])
     rows = np.unique(np.concatenate([ends, rng.integers(0, gin.M, 24)]))
     check_grouped(orc, gin, got, act=act, rows=rows, what=name)
+
+
+@pytest.mark.parametrize("fmt", ["nvfp4", "mxfp4"])
+def test_grouped_many_groups(fp4, orc, fmt):
+    # 256 groups (the most one call takes), most of them empty or a few rows,
+    # one large; K not a multiple of the 256-element k-tile
+    rng = np.random.default_rng(21)
+    sizes = np.where(rng.random(256) < 0.6, 0, rng.integers(1, 20, 256))
+    sizes[77] = 300
+    gin = W.make_grouped(fmt, sizes, 64, 288, seed=4)
+    got = run_grouped(fp4, gin)
+    rows = np.unique(np.concatenate([np.arange(0, gin.M, 7), [gin.M - 1]]))
+    check_grouped(orc, gin, got, rows=rows, what="256 groups %s" % fmt)

@@ -195,7 +195,7 @@ def config_names() -> list[str]:
     for m in PROJ_MS:
         names.append("nvfp4_proj_m%d_n14336_k4096" % m)
         names.append("nvfp4_proj_m%d_n4096_k14336" % m)
-    names += ["nvfp4_8191x3000x5120_f32", "nvfp4_1x28672x4096_f32"]
+    names += ["nvfp4_8191x3000x5120_f32", "nvfp4_1x28672x4096_f32", "nvfp4_8192_f32"]
     return names
 
 
@@ -215,6 +215,9 @@ def config_shape(name: str) -> dict:
         return dict(fmt="nvfp4", M=8191, N=3000, K=5120, out="f32", alpha=1.0)
     if name == "nvfp4_1x28672x4096_f32":
         return dict(fmt="nvfp4", M=1, N=28672, K=4096, out="f32", alpha=1.0)
+    if name == "nvfp4_8192_f32":
+        # the 8192^3 GEMM in the NVFP4 format (the MXFP4 workload's values, per-16 E4M3 scales)
+        return dict(fmt="nvfp4", M=8192, N=8192, K=8192, out="f32", alpha=1.0)
     raise KeyError(name)
 
 
