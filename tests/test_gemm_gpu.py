@@ -206,7 +206,7 @@ PLAN_CASES = [
     # (mode, bn, splits, cta_group): direct and swap-AB, both tile widths, one CTA
     # or a CTA pair per MMA, split-K
     (1, 256, 0, 1), (1, 128, 0, 1), (1, 256, 0, 2), (1, 128, 0, 2), (2, 256, 0, 1), (2, 128, 0, 1),
-    (2, 256, 0, 2), (2, 128, 2, 2), (2, 256, 3, 1), (2, 128, 2, 1), (2, 256, 3, 2), (1, 256, 0, 2),
+    (2, 256, 0, 2), (2, 128, 2, 2), (2, 128, 3, 1), (2, 128, 2, 1), (2, 256, 3, 2), (1, 256, 0, 2),
     (1, 64, 0, 1), (1, 32, 0, 1),
 ]
 
@@ -260,6 +260,17 @@ def test_mxfp4_pairs_k_lengths(fp4, orc, K):
     check_full(orc, inp, run(fp4, inp, fp4.GemmConfig(mode=1, bn=256, cta_group=2)), "direct K=%d" % K)
     check_full(orc, inp, run(fp4, inp, fp4.GemmConfig(mode=1, bn=128, cta_group=2)), "direct bn128 K=%d" % K)
     check_full(orc, inp, run(fp4, inp, fp4.GemmConfig(mode=2, bn=256, cta_group=2, splits=3)), "split K=%d" % K)
+
+
+@pytest.mark.parametrize("M,N,K,bn,splits", [(40, 2000, 4096, 64, 4), (16, 300, 14336, 16, 7), (100, 640, 2048, 128, 5),
+                                              (200, 136, 1024, 256, 3)])
+def test_split_k_plans(fp4, orc, M, N, K, bn, splits):
+    # forced K splits over tile widths 16 .. 256 (fixed summation order)
+    inp = W.make_random("nvfp4", M, N, K, out="f32", seed=M + splits)
+    cfg = fp4.GemmConfig(mode=2, bn=bn, splits=splits, cta_group=2 if bn == 256 else 1)
+    a = run(fp4, inp, cfg)
+    check_full(orc, inp, a, "split-K %s" % ((M, N, K, bn, splits),))
+    np.testing.assert_array_equal(a, run(fp4, inp, cfg))
 
 
 def test_prepacked_equals_plain(fp4, orc):
