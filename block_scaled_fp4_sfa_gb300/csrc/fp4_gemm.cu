@@ -157,7 +157,7 @@ struct Cfg {
     static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
     static constexpr int SLOTS = STAGES;
     static constexpr int ACC_BUFS = BN <= 128 ? 2 : 1;
-    static constexpr bool WAITER_COPIES = CG == 1 && !MX;   // who issues the scale copies (see the waiter warp)
+    static constexpr bool WAITER_COPIES = !MX;   // who issues the scale copies (see the waiter warp)
     static constexpr int SF_COLS = 4 * APK * (1 + NRB);        // TMEM columns of one k-tile's scales
     static constexpr int SF_TMEM = ACC_BUFS * BN;               // first scale column
     static constexpr int TMEM_USED = ACC_BUFS * BN + SLOTS * SF_COLS;
@@ -601,14 +601,14 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tmap_a, const CUten
         // the running count, so that the MMA thread blocks in an mbarrier wait
         // only once per tile (for the accumulator): on this part a wait in the
         // issuing thread costs about 200 cycles in which the tensor core runs
-        // dry. For NVFP4 with one CTA per MMA (twelve scale copies per k-tile)
-        // it also copies the stage's scale atoms into the stage's TMEM slot
-        // (tcgen05.cp) and waits for them before publishing, so that the copies
-        // overlap the MMAs of earlier stages instead of queueing behind them in
-        // the MMA thread (4096^3 55.4 -> 51.4 us, 8192 x 4096 x 14336
-        // 262 -> 236 us). MXFP4 (six copies per k-tile) keeps them in the MMA
-        // thread: there the split measured slower (8192^3 with CTA pairs
-        // 231 -> 287 us, with one CTA per MMA 250 -> 274 us).
+        // dry. For NVFP4 (twelve scale copies per k-tile) it also copies the
+        // stage's scale atoms into the stage's TMEM slot (tcgen05.cp) and waits
+        // for them before publishing, so that the copies overlap the MMAs of
+        // earlier stages instead of queueing behind them in the MMA thread (one
+        // CTA per MMA: 4096^3 55.4 -> 51.4 us, 8192 x 4096 x 14336 262 -> 236 us;
+        // CTA pairs: 8192^3 313 -> 299 us). MXFP4 (six copies per k-tile) keeps
+        // them in the MMA thread: there the split measured slower (8192^3 with
+        // CTA pairs 231 -> 287 us, with one CTA per MMA 250 -> 274 us).
         if (lane == 0 && rank == 0) {
             // scale atom: 32 rows of 16 bytes, 8-row groups 128 bytes apart
             const uint64_t desc_sfa0 = smem_desc(base + C::OFF_SFA, 0, 128, 0);
