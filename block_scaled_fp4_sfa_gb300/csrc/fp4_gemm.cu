@@ -1254,10 +1254,11 @@ int pow2_bn(int64_t rows)
 }
 
 // The narrow-M CUDA-core kernel: forced by mode 3 (M <= kGemvMaxM), or chosen
-// automatically where it measured faster than the tcgen05 path on 28672 x 4096:
-// M <= 2 with plain scales (it needs no scale reorder), M == 1 with prepacked
-// ones. Either way only when its shared staging of A fits and B's scales are
-// 2-byte aligned (it reads NVFP4 scale pairs as 16-bit words).
+// automatically where it measured faster than the tcgen05 path (one launch
+// instead of the scale reorder plus the GEMM): M == 1 with plain scales. On
+// prepacked scales, and from M = 2, the tcgen05 path measured faster on
+// 28672 x 4096. Either way only when its shared staging of A fits and B's
+// scales are 2-byte aligned (it reads NVFP4 scale pairs as 16-bit words).
 fp4_status choose_gemv(int64_t M, int64_t K, bool mx, int prepacked, const fp4_gemm_config *cfg, bool sfb_even,
                        bool &gemv)
 {
@@ -1266,7 +1267,7 @@ fp4_status choose_gemv(int64_t M, int64_t K, bool mx, int prepacked, const fp4_g
     const bool fits = gemv_smem_bytes(M, K, mx) != 0;
     if (mode == 3 && !fits) return FP4_ERR_UNSUPPORTED;
     if (mode == 3 && !sfb_even) return FP4_ERR_MISALIGNED;
-    gemv = mode == 3 || (mode == 0 && fits && sfb_even && M <= (prepacked ? 1 : 2));
+    gemv = mode == 3 || (mode == 0 && fits && sfb_even && !prepacked && M == 1);
     return FP4_OK;
 }
 

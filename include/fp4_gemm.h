@@ -77,11 +77,11 @@ typedef enum { FP4_FMT_NVFP4 = 0, FP4_FMT_MXFP4 = 1 } fp4_format;
  *              the CuTe DSL, part 1", section on the swapped operands);
  *              3 the narrow-M CUDA-core kernel (M <= 4; it reads both scale
  *              layouts in place, so it launches no reorder and needs no
- *              scratch; sfB must be 2-byte aligned). Auto picks 3 for M <= 2
- *              with plain scales and M == 1 with prepacked ones (where it
- *              measured faster), when A's decoded rows fit its shared staging
- *              (M * (K + K/vec * 4) bytes, K rounded up to 4096, at most
- *              200 KB) and sfB is 2-byte aligned; else 2 for M <= 256, else 1.
+ *              scratch; sfB must be 2-byte aligned). Auto picks 3 for M == 1
+ *              with plain scales (where it measured faster), when A's decoded
+ *              row fits its shared staging (K + K/vec * 4 bytes, K rounded up
+ *              to 4096, at most 200 KB) and sfB is 2-byte aligned; else 2 for
+ *              M <= 256, else 1.
  *              The other fields apply to modes 1 and 2 only.
  *   bn:        0 auto; else the MMA N of a tile: 16, 32, 64, 128 or 256.
  *              Direct mode needs 128 or 256; so do several tiles on the N side.
