@@ -6,8 +6,10 @@
 A step is one pass of the whole hot path over one problem, exactly what
 fp4_gemm_nvfp4 / fp4_gemm_mxfp4 launch, each a C-ABI call: the scale reorder
 of sfA and sfB into the 128x4 atom layout (one launch), then the persistent
-tcgen05 GEMM on the reordered scales; or, for the narrow-M plans, the CUDA-core
-kernel alone (it reads the plain scales in place). Inputs are seeded synthetic data resident in HBM; L2 is
+tcgen05 GEMM on the reordered scales; or, where the plan is a single launch
+(the narrow-M CUDA-core kernel, which reads the plain scales in place), that
+launch alone.
+Inputs are seeded synthetic data resident in HBM; L2 is
 flushed (a 256 MiB write) between timed steps, outside each step's events, and
 a spin kernel queued before each step keeps host launch overhead out of them.
 
@@ -265,12 +267,13 @@ def run_ours(args, inp, rank, ws, local, act=None, bias=None):
     dbias = hbias.to(dev) if bias is not None else None
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     s = stream.cuda_stream
-    # The narrow-M kernel reads plain scales in place: its step is the plain
-    # call alone. The tcgen05 GEMM's step is the two scale reorders the plain
-    # call would launch, then the GEMM on the reordered scales (timed alone).
+    # A plan of one launch (the narrow-M kernel) makes the step the plain call
+    # alone. Otherwise the step is the scale reorder the plain call would launch,
+    # then the GEMM on the reordered scales (timed alone).
     plan = fp4.gemm_plan(inp.fmt, inp.M, inp.N, inp.K, inp.out, act=act or "none")
     narrow = plan["kernel"] == "narrow"
-    pre = not narrow
+    single = plan["launches"] == 1
+    pre = not single
     call = ((fp4.gemm_nvfp4_prepacked if pre else fp4.gemm_nvfp4) if inp.fmt == "nvfp4"
             else (fp4.gemm_mxfp4_prepacked if pre else fp4.gemm_mxfp4))
 
@@ -287,7 +290,7 @@ def run_ours(args, inp, rank, ws, local, act=None, bias=None):
         torch.cuda._sleep(SPACER_CYCLES)
 
     def step():
-        if narrow:
+        if single:
             ev_g0.record(stream)
             gemm_call(A, sfA, B, sfB, D, dbias)
             ev_g1.record(stream)

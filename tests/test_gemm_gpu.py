@@ -273,6 +273,33 @@ def test_split_k_plans(fp4, orc, M, N, K, bn, splits):
     np.testing.assert_array_equal(a, run(fp4, inp, cfg))
 
 
+@pytest.mark.parametrize("M,N,K,cfg", [(300, 520, 1024, None), (768, 768, 1280, (1, 256, 1)), (40, 1000, 2048, (2, 64, 1)),
+                                       (16, 700, 4096, (2, 16, 1)), (200, 384, 768, (2, 256, 1)),
+                                       (129, 264, 512, (1, 128, 1)), (300, 520, 1056, None)])
+def test_nvfp4_plain_equals_prepacked(fp4, orc, M, N, K, cfg):
+    # plain NVFP4 scales (reordered by the call) against the prepacked call on the
+    # same plan: bit-identical, and within tolerance of the oracle
+    inp = W.make_random("nvfp4", M, N, K, out="f32", alpha=0.5, dist="t3", seed=M + K)
+    c = None if cfg is None else fp4.GemmConfig(mode=cfg[0], bn=cfg[1], cta_group=cfg[2])
+    plan = fp4.gemm_plan("nvfp4", M, N, K, "f32", config=c)
+    assert plan["launches"] == 2 + (1 if plan["splits"] > 1 else 0)
+    a = run(fp4, inp, c)
+    check_full(orc, inp, a, "plain scales %s" % ((M, N, K, cfg),))
+    np.testing.assert_array_equal(a, run(fp4, inp, c, prepacked=True))
+
+
+def test_nvfp4_plain_scales_unaligned(fp4, orc):
+    # scales at an address that is not 16-byte aligned (the reorder reads bytes)
+    inp = W.make_random("nvfp4", 300, 256, 512, out="f32", seed=2)
+    A, sfA, B, sfB = (_dev(getattr(inp, k)) for k in ("A", "sfA", "B", "sfB"))
+    buf = torch.zeros(inp.sfA.size + 4, dtype=torch.uint8, device="cuda")
+    buf[4:] = torch.from_numpy(inp.sfA.reshape(-1)).cuda()
+    D = torch.full((inp.M, inp.N), float("nan"), device="cuda")
+    fp4.gemm("nvfp4", A, buf.data_ptr() + 4, B, sfB, inp.alpha, D, inp.M, inp.N, inp.K, "f32")
+    assert fp4.get_device_status() == fp4.FP4_OK
+    check_full(orc, inp, D.cpu().numpy().astype(np.float64), "unaligned scales")
+
+
 def test_prepacked_equals_plain(fp4, orc):
     inp = W.make_random("mxfp4", 300, 520, 768, out="f32", seed=4)
     a = run(fp4, inp)

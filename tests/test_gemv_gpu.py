@@ -124,7 +124,7 @@ def test_plan_choice(fp4):
     assert fp4.gemm_plan("nvfp4", 4, 100, 4096, config=fp4.GemmConfig(mode=3))["kernel"] == "narrow"
     assert fp4.gemm_plan("nvfp4", 1, 100, 4096, config=fp4.GemmConfig(mode=2))["kernel"] == "tcgen05"
     p = fp4.gemm_plan("nvfp4", 4096, 4096, 4096, "bf16")
-    assert p["kernel"] == "tcgen05" and not p["swap"] and p["launches"] == 2
+    assert p["kernel"] == "tcgen05" and not p["swap"] and p["launches"] == 2     # reorder + GEMM
     assert fp4.gemm_plan("nvfp4", 4096, 4096, 4096, "bf16", prepacked=True)["launches"] == 1
     with pytest.raises(fp4.Fp4Error):
         fp4.gemm_plan("nvfp4", 5, 100, 4096, config=fp4.GemmConfig(mode=3))     # M > 4

@@ -74,10 +74,17 @@ def test_static_scratch_matches_allocating_entry(fp4, fmt, M, N, K, out):
 
 
 def test_static_scratch_rejects_oversized(fp4):
-    # 2 x 65536 rows x 256 atoms/row-block... scales alone exceed 16 MiB
-    M = N = 1 << 16
-    K = 1 << 14
-    z = torch.zeros(16, dtype=torch.uint8, device="cuda")
-    st = fp4.gemm_static_scratch("nvfp4", z, z, z, z, 1.0, z, M, N, K, "f32", check=False)
+    # MXFP4 always reorders its scales: at 8192 x 8192 x 65536 the two atom copies
+    # take 2 x 64 row blocks x 512 atoms x 512 B = 32 MiB, over the 16 MiB array.
+    # Every buffer is real and sized for the problem (all zeros), so the call is
+    # a valid GEMM even if it were not refused.
+    M = N = 8192
+    K = 1 << 16
+    A = torch.zeros(M, K // 2, dtype=torch.uint8, device="cuda")
+    B = torch.zeros(N, K // 2, dtype=torch.uint8, device="cuda")
+    sfA = torch.zeros(M, K // 32, dtype=torch.uint8, device="cuda")
+    sfB = torch.zeros(N, K // 32, dtype=torch.uint8, device="cuda")
+    D = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+    st = fp4.gemm_static_scratch("mxfp4", A, sfA, B, sfB, 1.0, D, M, N, K, "bf16", check=False)
     assert st == 7 and "static scratch" in fp4.status_string(st)
     assert fp4.get_device_status() == fp4.FP4_OK
