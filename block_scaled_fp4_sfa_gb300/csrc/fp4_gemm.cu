@@ -13,14 +13,23 @@
 //   warp 0      TMA producer (one thread): fills a ring of shared-memory
 //               stages; a stage is one k-tile (256 FP4 elements = 128 bytes
 //               per row) of both operands (128B-swizzled) and their scale atoms;
-//   warp 1      MMA issuer (one thread of the leader CTA): copies the stage's
-//               scale atoms into TMEM (tcgen05.cp) and issues four K = 64
-//               block-scaled MMAs into a TMEM accumulator, then frees the stage;
+//   warp 10     waiter (one thread of the leader CTA): waits for each stage to
+//               land and publishes the count to the MMA thread; for NVFP4 it
+//               first copies the stage's scale atoms into TMEM (tcgen05.cp);
+//   warp 1      MMA issuer (one thread of the leader CTA): for MXFP4 copies the
+//               scale atoms, then issues four K = 64 block-scaled MMAs into a
+//               TMEM accumulator and frees the stage;
 //   warps 2..9  epilogue: each warp drains its 32 TMEM lanes x BN/2 columns
 //               into registers, hands the accumulator back at once, then
-//               scales, casts and stores (a per-warp 128B-swizzled TMA store
-//               box, coalesced stores of the transposed tile for swap-AB, or
-//               fp32 split-K partials) while the next tile's MMAs run.
+//               applies alpha, the bias and the activation (fp4_gemm_fused),
+//               casts and stores -- rows through a per-warp staging buffer in
+//               whole 32-byte sectors, or the transposed tile for swap-AB, or
+//               fp32 split-K partials -- while the next tile's MMAs run.
+//
+// Every launch may start as a programmatic dependent of the scale reorder
+// before it; all threads wait for that grid before touching memory. The
+// grouped GEMM (fp4_gemm_grouped) instantiates the same body with its groups'
+// geometry in the parameter block.
 //
 // CG = 2 runs a CTA pair (cluster of 2) on one 256-row MMA (tcgen05
 // cta_group::2): each CTA loads 128 rows of the M side and half of the N side,

@@ -71,8 +71,8 @@ typedef enum { FP4_OUT_F32 = 0, FP4_OUT_BF16 = 1 } fp4_out_dtype;
 typedef enum { FP4_FMT_NVFP4 = 0, FP4_FMT_MXFP4 = 1 } fp4_format;
 
 /* Optional overrides of the launch plan (zero-initialise for "automatic").
- *   mode:      0 auto; 1 direct (A on the MMA's M side, D written by TMA
- *              stores); 2 swap-AB (B on the M side, D^T tiles written with
+ *   mode:      0 auto; 1 direct (A on the MMA's M side, D rows written in
+ *              whole 32-byte sectors); 2 swap-AB (B on the M side, D^T tiles written with
  *              coalesced stores; the trick of "Hopper GEMM in CUTLASS C++ and
  *              the CuTe DSL, part 1", section on the swapped operands);
  *              3 the narrow-M CUDA-core kernel (M <= 4; it reads both scale
