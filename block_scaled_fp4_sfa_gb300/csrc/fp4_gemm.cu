@@ -1130,6 +1130,7 @@ cudaError_t launch_gemm(DeviceInfo &info, int kidx, int units, int cap, const Ma
     cluster_attr[0].val.clusterDim.z = 1;
     cluster_attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     cluster_attr[1].val.programmaticStreamSerializationAllowed = 1;
+    std::unique_lock<std::mutex> lk(g_mu);      // (calls from several host threads)
     if (!info.attr_set[kidx]) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
         if (e != cudaSuccess) return e;
@@ -1152,6 +1153,7 @@ cudaError_t launch_gemm(DeviceInfo &info, int kidx, int units, int cap, const Ma
         info.attr_set[kidx] = true;
     }
     const int slots = info.max_clusters[kidx];
+    lk.unlock();
     if (slots_out) {
         *slots_out = cap > 0 ? std::max(1, std::min(slots, cap / CG)) : slots;
         return cudaSuccess;
