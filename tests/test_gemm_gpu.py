@@ -400,3 +400,32 @@ def test_error_statuses_launch_nothing(fp4):
     assert g("nvfp4", z, z, z, z, 1.0, D, 64, 64, 64, "f32", config=fp4.GemmConfig(cta_group=3)) == 1
     assert g("nvfp4", z, z, z, z, 1.0, D, 64, 64, 64, "f32", config=fp4.GemmConfig(bn=64, cta_group=2)) == 2
     assert fp4.get_device_status() == 0
+
+
+def test_two_host_threads_two_streams(fp4, orc):
+    # calls from two host threads on their own streams, first use of several
+    # kernel variants racing: every result matches the oracle
+    import threading
+    cases = [W.make_random("nvfp4", 300, 520, 512, out="f32", seed=31),
+             W.make_random("mxfp4", 64, 777, 1024, out="bf16", seed=32)]
+    refs = [orc.gemm_rows(inp) for inp in cases]
+    results, errors = {}, []
+
+    def worker(i):
+        try:
+            s = torch.cuda.Stream()
+            with torch.cuda.stream(s):
+                for rep in range(3):
+                    results[(i, rep)] = run(fp4, cases[i], None)
+        except Exception as e:          # reported below
+            errors.append(repr(e))
+
+    ts = [threading.Thread(target=worker, args=(i,)) for i in range(2)]
+    for t in ts:
+        t.start()
+    for t in ts:
+        t.join(120)
+    assert not errors, errors
+    for (i, rep), got in results.items():
+        ref, absd = refs[i]
+        check_values(orc, cases[i].out, got, ref, absd, "thread %d rep %d" % (i, rep))
