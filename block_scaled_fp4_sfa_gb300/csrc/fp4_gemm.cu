@@ -1015,6 +1015,18 @@ int64_t g_wait_ms = -1;
 std::atomic<unsigned long long> g_epoch{0};   // per-launch value of the split-tail flags
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
+// True when work issued to `stream` is being recorded into a CUDA graph (or
+// when that cannot be told, so the caller takes the safe branch).
+bool stream_capturing(cudaStream_t stream)
+{
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) {
+        (void)cudaGetLastError();   // not sticky: keep it out of the launch checks
+        return true;
+    }
+    return cs != cudaStreamCaptureStatusNone;
+}
+
 constexpr int kNumKernels = 22;   // kernel variants that can be launched (see kernel_index)
 struct DeviceInfo {
     bool probed = false;
@@ -1513,6 +1525,15 @@ fp4_status gemm_impl(fp4_format fmt, int prepacked, const void *A, const void *s
     }
     fp4_status result = FP4_OK;
     do {
+        // A split-tail flag only ever matches its own launch's epoch, which a
+        // plain call never repeats. A captured call's epoch is replayed with the
+        // graph, so the flags a replay left behind would already match: zero them
+        // first (ahead of the reorder, which the GEMM follows as a dependent launch).
+        if (tail && stream_capturing(stream) &&
+            cudaMemsetAsync(scratch + tail_off + tail_ws_bytes, 0, tail_flag_bytes, stream) != cudaSuccess) {
+            result = FP4_ERR_CUDA;
+            break;
+        }
         const uint8_t *sfa_atoms = static_cast<const uint8_t *>(sf_a);
         const uint8_t *sfb_atoms = static_cast<const uint8_t *>(sf_b);
         uint8_t *ws = scratch + (prepacked ? 0 : atoms_a + atoms_b);

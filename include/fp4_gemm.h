@@ -44,6 +44,14 @@
  * bounded; a wait that runs out records FP4_ERR_TIMEOUT in a per-device status
  * word that fp4_get_device_status reports. Calls are asynchronous with respect
  * to the host and run on the current device.
+ *
+ * Graphs: the GEMM, reorder and quantiser calls may be recorded by stream
+ * capture into a CUDA graph, once a plain call of the same kind has run on the
+ * device (it sets the kernels' attributes). Each replay repeats the captured
+ * plan on the same buffers, alpha and (grouped calls) group offsets, and reads
+ * whatever the input buffers hold at replay time. Scratch taken while capturing
+ * becomes graph-owned memory. fp4_get_device_status synchronises the stream and
+ * cannot be captured.
  */
 #ifndef FP4_GEMM_H
 #define FP4_GEMM_H
