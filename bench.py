@@ -3,12 +3,16 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload NAME] [--results PATH]
 
-A step is one pass of the whole hot path over one problem, exactly what
-fp4_gemm_nvfp4 / fp4_gemm_mxfp4 launch, each a C-ABI call: the scale reorder
-of sfA and sfB into the 128x4 atom layout (one launch), then the persistent
-tcgen05 GEMM on the reordered scales; or, where the plan is a single launch
-(the narrow-M CUDA-core kernel, which reads the plain scales in place), that
-launch alone.
+A step is one pass of the whole hot path over one problem: one call of
+fp4_gemm_nvfp4 / fp4_gemm_mxfp4 (the C ABI) on plain scales. The call reorders
+sfA and sfB into the 128x4 atom layout (one launch), then launches the
+persistent tcgen05 GEMM on the reordered scales as a programmatic dependent of
+the reorder; where the plan is a single launch (the narrow-M CUDA-core kernel,
+which reads the plain scales in place), that launch alone. Nothing is recorded
+between the reorder and the GEMM (an event there would break their overlap),
+so the GEMM's own duration, for the roofline, is timed separately: the GEMM
+alone on scales reordered once before the loop, launched between the timed
+steps after its own L2 flush, with CUDA events around it.
 Inputs are seeded synthetic data resident in HBM; L2 is
 flushed (a 256 MiB write) between timed steps, outside each step's events, and
 a spin kernel queued before each step keeps host launch overhead out of them.
@@ -34,11 +38,11 @@ GEMM plus its epilogue as the cpu_baseline and e2e through pinned host
 buffers copied on the stream around the same call.
 
 --op grouped times the grouped (mixture-of-experts) GEMM, fp4_gemm_grouped,
-on the moe_* workloads: a step is the grouped reorder of the routed
-activations' scales, the reorder of the experts' weight scales and the one
-grouped GEMM launch over all experts (timed alone for the roofline; its
-events also cover the few-KB copy of the per-group tables). Same metric
-(2 * M_total * N * K per step).
+on the moe_* workloads: a step is one grouped call on plain scales (one
+reorder launch for the routed activations' and the experts' weight scales,
+then the one grouped GEMM launch over all experts); the GEMM alone on
+prepacked scales is timed between the steps for the roofline, as above. Same
+metric (2 * M_total * N * K per step).
 
 --op quantize measures the quantisation step that feeds the GEMM instead
 (fp4_quantize: bf16 or fp32 activations -> E2M1 codes + atom-layout scales),
@@ -267,22 +271,27 @@ def run_ours(args, inp, rank, ws, local, act=None, bias=None):
     dbias = hbias.to(dev) if bias is not None else None
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     s = stream.cuda_stream
-    # A plan of one launch (the narrow-M kernel) makes the step the plain call
-    # alone. Otherwise the step is the scale reorder the plain call would launch,
-    # then the GEMM on the reordered scales (timed alone).
+    # The step is the call a user makes on plain scales: it reorders them and
+    # launches the GEMM as a programmatic dependent of the reorder. The GEMM's
+    # own duration (for the roofline) is timed alone, on scales reordered once
+    # before the loop, between the timed steps and after its own L2 flush: an
+    # event recorded between the reorder and the GEMM would break their overlap.
+    # A plan of one launch (the narrow-M kernel reads plain scales in place)
+    # needs no second leg: the step is the kernel.
     plan = fp4.gemm_plan(inp.fmt, inp.M, inp.N, inp.K, inp.out, act=act or "none")
     narrow = plan["kernel"] == "narrow"
     single = plan["launches"] == 1
-    pre = not single
-    call = ((fp4.gemm_nvfp4_prepacked if pre else fp4.gemm_nvfp4) if inp.fmt == "nvfp4"
-            else (fp4.gemm_mxfp4_prepacked if pre else fp4.gemm_mxfp4))
+    kplan = fp4.gemm_plan(inp.fmt, inp.M, inp.N, inp.K, inp.out, act=act or "none", prepacked=True)
+    leg_launches = 0 if single else kplan["launches"]
+    plain_call = fp4.gemm_nvfp4 if inp.fmt == "nvfp4" else fp4.gemm_mxfp4
+    pre_call = fp4.gemm_nvfp4_prepacked if inp.fmt == "nvfp4" else fp4.gemm_mxfp4_prepacked
 
-    def gemm_call(a, sa, b, sb, d, bb):
+    def gemm_call(a, sa, b, sb, d, bb, pre):
         if fused:
             fp4.gemm_fused(inp.fmt, a, sa, b, sb, inp.alpha, d, inp.M, inp.N, inp.K, inp.out, act=act, bias=bb,
                            prepacked=pre, stream=s)
         else:
-            call(a, sa, b, sb, inp.alpha, d, inp.M, inp.N, inp.K, inp.out, stream=s)
+            (pre_call if pre else plain_call)(a, sa, b, sb, inp.alpha, d, inp.M, inp.N, inp.K, inp.out, stream=s)
 
     def spacer():
         # a spin kernel keeps the GPU busy while the host enqueues the step, so no
@@ -290,22 +299,21 @@ def run_ours(args, inp, rank, ws, local, act=None, bias=None):
         torch.cuda._sleep(SPACER_CYCLES)
 
     def step():
-        if single:
-            ev_g0.record(stream)
-            gemm_call(A, sfA, B, sfB, D, dbias)
-            ev_g1.record(stream)
-            return
-        fp4.scale_reorder2(sfA, atomA, inp.M, sfB, atomB, inp.N, inp.K, vec, stream=s)
-        ev_g0.record(stream)
-        gemm_call(A, atomA, B, atomB, D, dbias)
-        ev_g1.record(stream)
+        gemm_call(A, sfA, B, sfB, D, dbias, False)
 
-    ev_g0 = torch.cuda.Event(enable_timing=True)
-    ev_g1 = torch.cuda.Event(enable_timing=True)
+    def kernel_alone():
+        gemm_call(A, atomA, B, atomB, D, dbias, True)
+
+    if not single:
+        fp4.scale_reorder2(sfA, atomA, inp.M, sfB, atomB, inp.N, inp.K, vec, stream=s)
     for _ in range(args.warmup):
         flush.zero_()
         spacer()
         step()
+        if not single:
+            flush.zero_()
+            spacer()
+            kernel_alone()
     torch.cuda.synchronize()
     st = fp4.get_device_status(s)
     if st != 0:
@@ -313,8 +321,8 @@ def run_ours(args, inp, rank, ws, local, act=None, bias=None):
 
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    g0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    g1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    g0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)] if not single else starts
+    g1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)] if not single else ends
     if ws > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
@@ -325,9 +333,14 @@ def run_ours(args, inp, rank, ws, local, act=None, bias=None):
             flush.zero_()
             spacer()
             starts[i].record(stream)
-            ev_g0, ev_g1 = g0[i], g1[i]
             step()
             ends[i].record(stream)
+            if not single:
+                flush.zero_()
+                spacer()
+                g0[i].record(stream)
+                kernel_alone()
+                g1[i].record(stream)
         torch.cuda.synchronize()
         t_wall = time.perf_counter() - t_wall0
         if ws > 1:
@@ -402,7 +415,9 @@ def run_ours(args, inp, rank, ws, local, act=None, bias=None):
                     "peak_source": "%s bf16 burst %.1f TFLOP/s x %.0f (nominal FP4:bf16)" % (
                         peak_src, bf16_peak, FP4_PER_BF16)}
     roofline.update({"kernel": kname, "gemm_us": 1e3 * gemm_avg_ms, "algorithmic_bytes": alg_bytes,
-                     "hbm_frac_at_algorithmic_bytes": achieved_gbs / hbm_peak})
+                     "hbm_frac_at_algorithmic_bytes": achieved_gbs / hbm_peak,
+                     "timed": "the step itself" if single else
+                     "alone on prepacked scales, between the timed steps, L2 flushed before each launch"})
     result = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
@@ -411,7 +426,7 @@ def run_ours(args, inp, rank, ws, local, act=None, bias=None):
         "roofline": roofline,
         "e2e": {"value": inp.flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
-        "gpu_launches": plan["launches"] * args.steps,
+        "gpu_launches": (plan["launches"] + leg_launches) * args.steps,
         "clocks": clk.summary(),
         "wall_s_timed_region": t_wall,
     }
@@ -558,20 +573,24 @@ def run_grouped(args, rank, ws, local):
     D = torch.empty(M, d_cols, dtype=odt, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
 
+    # The step is the grouped call on plain scales (one reorder launch for the
+    # routed activations' and the experts' scales, then the GEMM as its
+    # programmatic dependent). The GEMM alone, on scales reordered once before
+    # the loop, is timed between the steps for the roofline.
     def step():
-        fp4.scale_reorder_grouped(sfA, atomA, gin.offsets, K, vec, stream=s)
-        fp4.scale_reorder(sfB, atomB, G * N, K, vec, stream=s)
-        ev_g0.record(stream)
+        fp4.gemm_grouped(gin.fmt, gin.offsets, A, sfA, B, sfB, gin.alpha, D, N, K, gin.out, act=act, stream=s)
+
+    def kernel_alone():
         fp4.gemm_grouped(gin.fmt, gin.offsets, A, atomA, B, atomB, gin.alpha, D, N, K, gin.out, act=act,
                          weights_prepacked=True, acts_prepacked=True, stream=s)
-        ev_g1.record(stream)
 
-    ev_g0 = torch.cuda.Event(enable_timing=True)
-    ev_g1 = torch.cuda.Event(enable_timing=True)
+    fp4.scale_reorder_grouped(sfA, atomA, gin.offsets, K, vec, stream=s)
+    fp4.scale_reorder(sfB, atomB, G * N, K, vec, stream=s)
     for _ in range(args.warmup):
-        flush.zero_()
-        torch.cuda._sleep(SPACER_CYCLES)
-        step()
+        for f in (step, kernel_alone):
+            flush.zero_()
+            torch.cuda._sleep(SPACER_CYCLES)
+            f()
     torch.cuda.synchronize()
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
@@ -586,9 +605,13 @@ def run_grouped(args, rank, ws, local):
             flush.zero_()
             torch.cuda._sleep(SPACER_CYCLES)
             starts[i].record(stream)
-            ev_g0, ev_g1 = g0[i], g1[i]
             step()
             ends[i].record(stream)
+            flush.zero_()
+            torch.cuda._sleep(SPACER_CYCLES)
+            g0[i].record(stream)
+            kernel_alone()
+            g1[i].record(stream)
         torch.cuda.synchronize()
         if ws > 1:
             torch.distributed.barrier()
@@ -656,7 +679,7 @@ def run_grouped(args, rank, ws, local):
         "e2e": {"value": gin.flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in (hA, hsA, hB, hsB)),
                 "d2h_bytes_per_step": pD.numel() * pD.element_size()},
-        "gpu_launches": 3 * args.steps,
+        "gpu_launches": 3 * args.steps,      # step: reorder + GEMM; then the GEMM alone
         "clocks": clk.summary(),
     })
     if rank == 0 and not args.no_cpu_baseline:
