@@ -36,8 +36,9 @@
  *
  * Ownership: the caller owns every buffer; the library never frees them.
  * Calls taking plain scales reorder them into stream-ordered scratch
- * (cudaMallocAsync / cudaFreeAsync on `stream`); split-K partial sums use the
- * same kind of scratch. Nothing else is allocated per call.
+ * (cudaMallocAsync / cudaFreeAsync on `stream`); the partial sums of split-K
+ * plans and of a split last wave (with its hand-off flags) use the same kind
+ * of scratch. Nothing else is allocated per call.
  *
  * Errors: argument problems return a status synchronously and launch nothing.
  * Launch failures return FP4_ERR_CUDA. Every wait inside the kernels is
