@@ -257,9 +257,12 @@ fp4_status fp4_gemm_host(fp4_format fmt, const void *A, const void *sfA, const v
  * for split-K plans, splits * M * N * 4 bytes) are rejected with
  * FP4_ERR_SCRATCH_LIMIT before anything is launched. The call allocates
  * nothing and calls no allocating library routine. Nothing in the array has
- * to start at zero: every byte a call reads was written earlier in the same
- * call. All calls on a device share the array, so calls whose kernels overlap
- * on the GPU (other streams, other threads) race: order them on one stream.
+ * to start at zero. Every data byte a call reads was written earlier in the
+ * same call. The one exception is the split last wave's hand-off flags, which
+ * count as raised only when they hold that launch's own 64-bit epoch (a value
+ * no earlier call used). All calls on a device share the array, so calls
+ * whose kernels overlap on the GPU (other streams, other threads) race: order
+ * them on one stream.
  * The first call on a device looks up the array's device address
  * (cudaGetSymbolAddress) with that device current; make that first call
  * before any stream capture. Inputs, outputs and errors as fp4_gemm. */
