@@ -70,7 +70,7 @@ if ROOT not in sys.path:
 import workloads as W  # noqa: E402
 
 METRIC = "block-scaled FP4 GEMM TFLOP/s on 1 GB300 and % of dense FP4 tensor peak"
-DEFAULT_WORKLOAD = "nvfp4_4096_bf16"
+DEFAULT_WORKLOAD = "nvfp4_8192_f32"
 DEFAULT_FUSED_WORKLOAD = "ffn_swiglu_nvfp4_m8192_n28672_k4096"
 DEFAULT_GROUPED_WORKLOAD = "moe_nvfp4_e64_t4096_top8_n2048_k4096"
 FP4_PER_BF16 = 13.5 / 2.25       # nominal dense FP4 : dense bf16 tensor throughput on GB300
@@ -132,28 +132,37 @@ def ncu_traffic(workload, sources=GEMM_SOURCES):
 
 
 class ClockSampler:
-    """nvidia-smi clock / throttle sampling while the timed region runs."""
-    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi clock / throttle sampling (every 20 ms) while the timed region
+    runs; only samples stamped inside the region (mark_start / mark_end) count."""
+    Q = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
 
     def __init__(self, index):
         self.index = index
         self.proc = None
+        self.t0 = self.t1 = None
+        self.lines = []
 
     def __enter__(self):
         if self.index < 0:
             return self
         try:
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.Q,
-                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                          "--format=csv,noheader,nounits", "-lms", "20"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
         return self
 
+    def mark_start(self):
+        self.t0 = time.time()
+
+    def mark_end(self):
+        self.t1 = time.time()
+
     def __exit__(self, *exc):
-        self.lines = []
         if self.proc is not None:
             self.proc.terminate()
             try:
@@ -163,19 +172,29 @@ class ClockSampler:
                 out, _ = self.proc.communicate()
             self.lines = [l for l in out.splitlines() if l.strip()]
 
+    @staticmethod
+    def _stamp(text):
+        try:
+            whole, _, frac = text.strip().partition(".")
+            return time.mktime(time.strptime(whole, "%Y/%m/%d %H:%M:%S")) + float("0." + (frac or "0"))
+        except ValueError:
+            return None
+
     def summary(self):
         sm, mx, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for l in getattr(self, "lines", []):
+        for l in self.lines:
             f = [x.strip() for x in l.split(",")]
-            if len(f) < 9:
+            if len(f) < 10:
+                continue
+            ts = self._stamp(f[0])
+            if ts is None or self.t0 is None or not (self.t0 <= ts <= (self.t1 or ts)):
                 continue
             try:
-                sm.append(float(f[1]))
-                mx.append(float(f[2]))
+                sm.append(float(f[2]))
+                mx.append(float(f[3]))
             except ValueError:
                 continue
-            for n, v in zip(names, f[5:9]):
+            for n, v in zip(self.NAMES, f[6:10]):
                 if v.lower().startswith("active"):
                     reasons.add(n)
         if not sm:
@@ -221,7 +240,8 @@ def run_reference(args, inp):
     return {"metric": METRIC, "value": value, "unit": "TFLOP/s", "impl": "reference", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sum(times) / len(times),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": workload_config(inp),
+            "data": "synthetic",
+            "config": dict(workload_config(inp), parallelism="replicas" if args.gpus > 1 else "single"),
             "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
@@ -326,11 +346,14 @@ def run_ours(args, inp, rank, ws, local, act=None, bias=None):
     if ws > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
+    sp0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     with ClockSampler(local if not args.quick else -1) as clk:
-        time.sleep(0.2)
+        time.sleep(0.5)
+        clk.mark_start()
         t_wall0 = time.perf_counter()
         for i in range(args.steps):
             flush.zero_()
+            sp0[i].record(stream)
             spacer()
             starts[i].record(stream)
             step()
@@ -343,6 +366,7 @@ def run_ours(args, inp, rank, ws, local, act=None, bias=None):
                 g1[i].record(stream)
         torch.cuda.synchronize()
         t_wall = time.perf_counter() - t_wall0
+        clk.mark_end()
         if ws > 1:
             torch.distributed.barrier()
     st = fp4.get_device_status(s)
@@ -350,6 +374,8 @@ def run_ours(args, inp, rank, ws, local, act=None, bias=None):
         raise RuntimeError("device status after timing: %s" % fp4.status_string(st))
     step_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
     gemm_ms = [a.elapsed_time(b) for a, b in zip(g0, g1)]
+    # SM clock between the steps: the spin kernel runs SPACER_CYCLES clock cycles
+    spin_mhz = statistics.median(SPACER_CYCLES / (a.elapsed_time(b) * 1e3) for a, b in zip(sp0, starts))
     total_ms = slowest_rank_ms(sum(step_ms), ws, dev)
     ms_per_step = total_ms / args.steps
     value = whole_job_tflops(inp.flops, args.steps, ws, total_ms)
@@ -414,7 +440,12 @@ def run_ours(args, inp, rank, ws, local, act=None, bias=None):
                     "frac": achieved / fp4_peak, "traffic": traffic,
                     "peak_source": "%s bf16 burst %.1f TFLOP/s x %.0f (nominal FP4:bf16)" % (
                         peak_src, bf16_peak, FP4_PER_BF16)}
+    clocks = clk.summary()
+    clocks["sm_mhz_spin"] = spin_mhz
+    mhz = clocks["sm_mhz"] or spin_mhz
     roofline.update({"kernel": kname, "gemm_us": 1e3 * gemm_avg_ms, "algorithmic_bytes": alg_bytes,
+                     # kernel time x median SM clock = its cycles, so runs at other clocks compare
+                     "gemm_us_x_sm_mhz": 1e3 * gemm_avg_ms * mhz, "sm_mhz_used": mhz,
                      "hbm_frac_at_algorithmic_bytes": achieved_gbs / hbm_peak,
                      "timed": "the step itself" if single else
                      "alone on prepacked scales, between the timed steps, L2 flushed before each launch"})
@@ -427,7 +458,7 @@ def run_ours(args, inp, rank, ws, local, act=None, bias=None):
         "e2e": {"value": inp.flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": (plan["launches"] + leg_launches) * args.steps,
-        "clocks": clk.summary(),
+        "clocks": clocks,
         "wall_s_timed_region": t_wall,
     }
     return result
@@ -476,7 +507,8 @@ def run_quant(args, rank, ws, local):
         torch.distributed.barrier()
     torch.cuda.synchronize()
     with ClockSampler(local if not args.quick else -1) as clk:
-        time.sleep(0.2)
+        time.sleep(0.5)
+        clk.mark_start()
         for e0, e1 in ev:
             flush.zero_()
             torch.cuda._sleep(SPACER_CYCLES)
@@ -484,6 +516,7 @@ def run_quant(args, rank, ws, local):
             step()
             e1.record(stream)
         torch.cuda.synchronize()
+        clk.mark_end()
         if ws > 1:
             torch.distributed.barrier()
     st = fp4.get_device_status(s)
@@ -600,7 +633,8 @@ def run_grouped(args, rank, ws, local):
         torch.distributed.barrier()
     torch.cuda.synchronize()
     with ClockSampler(local if not args.quick else -1) as clk:
-        time.sleep(0.2)
+        time.sleep(0.5)
+        clk.mark_start()
         for i in range(args.steps):
             flush.zero_()
             torch.cuda._sleep(SPACER_CYCLES)
@@ -613,6 +647,7 @@ def run_grouped(args, rank, ws, local):
             kernel_alone()
             g1[i].record(stream)
         torch.cuda.synchronize()
+        clk.mark_end()
         if ws > 1:
             torch.distributed.barrier()
     st = fp4.get_device_status(s)

@@ -13,12 +13,10 @@
 //   warp 0      TMA producer (one thread): fills a ring of shared-memory
 //               stages; a stage is one k-tile (256 FP4 elements = 128 bytes
 //               per row) of both operands (128B-swizzled) and their scale atoms;
-//   warp 10     waiter (one thread of the leader CTA): waits for each stage to
-//               land and publishes the count to the MMA thread; for NVFP4 it
-//               first copies the stage's scale atoms into TMEM (tcgen05.cp);
-//   warp 1      MMA issuer (one thread of the leader CTA): for MXFP4 copies the
-//               scale atoms, then issues four K = 64 block-scaled MMAs into a
-//               TMEM accumulator and frees the stage;
+//   warp 1      MMA issuer (one thread of the leader CTA): waits for the stage
+//               to land, copies its scale atoms into TMEM (tcgen05.cp), issues
+//               four K = 64 block-scaled MMAs into a TMEM accumulator and frees
+//               the stage;
 //   warps 2..9  epilogue: each warp drains its 32 TMEM lanes x BN/2 columns
 //               into registers, hands the accumulator back at once, then
 //               applies alpha, the bias and the activation (fp4_gemm_fused),
@@ -56,10 +54,12 @@
 
 #include <algorithm>
 #include <atomic>
+#include <chrono>
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
+#include <random>
 #include <vector>
 
 #include "epilogue.cuh"
@@ -82,10 +82,23 @@ constexpr int kBM = 128;          // TMEM lanes / M rows per CTA
 constexpr int kBK = 256;          // FP4 elements per k-tile
 constexpr int kBKBytes = 128;     // bytes per row per k-tile
 constexpr int kAtomBytes = 512;   // one 128-row x 4-column scale atom
+// Warp roles, by warpgroup (4 warps): 0 = the TMA producer (warp 0), the MMA
+// issuer (warp 1) and two idle warps; 1-2 = eight epilogue warps; 3-4 = eight
+// scale warps. The epilogue warpgroups raise their registers to kEpiRegs (all
+// BN/2 accumulator columns of a warp fit in registers, so the accumulator is
+// handed back right after one drain) and the other three lower theirs to
+// kLowRegs, within the pool of kLaunchRegs per thread the block is launched
+// with (the host checks that count before the first launch).
 constexpr int kEpiWarps = 8;
-constexpr int kWaiterWarp = 2 + kEpiWarps;
-constexpr int kThreads = 32 * (kWaiterWarp + 1);   // producer, MMA, epilogue warps, waiter warp
-constexpr int kStgBytes = 32 * 32;              // per-warp store staging: 32 rows x 32 bytes
+constexpr int kSfWarps = 8;                      // scale warps: two per TMEM lane quarter
+constexpr int kFirstEpiWarp = 4;
+constexpr int kFirstSfWarp = kFirstEpiWarp + kEpiWarps;
+constexpr int kThreads = 32 * (kFirstSfWarp + kSfWarps);   // 640
+constexpr int kLaunchRegs = 96;
+constexpr int kEpiRegs = 168;
+constexpr int kLowRegs = 48;
+static_assert(kThreads % 128 == 0, "roles are whole warpgroups");
+static_assert(3 * 128 * kLowRegs + 2 * 128 * kEpiRegs <= kLaunchRegs * kThreads, "register split fits the pool");
 constexpr int kSmemLimit = 232448;
 
 enum EpiMode : int32_t { kEpiRows = 0, kEpiTransposed = 1, kEpiSplitK = 2 };
@@ -145,6 +158,8 @@ struct Args {
     float *tail_ws;                      // [tail tile][CTA of the pair][BN][128]
     unsigned long long *tail_flags;      // [tail tile][CTA of the pair]
     unsigned long long epoch;            // this launch's flag value
+    int32_t stop_after;                  // > 0: producers stop after this many stages (bounded-wait test)
+    int32_t st32;                        // rows mode: D and its row pitch 32-byte aligned (256-bit stores)
 };
 
 template <int CG, int BN, bool MX>
@@ -159,14 +174,14 @@ struct Cfg {
     static constexpr int SFB_BYTES = NRB * APK * kAtomBytes;
     static constexpr int KTILE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
     static constexpr int STAGE_BYTES = KTILE_BYTES;   // a stage is one k-tile
-    static constexpr int BAR_BYTES = 256;
-    static constexpr int STAGING_BYTES = kEpiWarps * kStgBytes;     // 8 KB
-    static constexpr int BUDGET = kSmemLimit - 1024 - BAR_BYTES - STAGING_BYTES;
+    static constexpr int BAR_BYTES = 512;
+    static constexpr int BUDGET = kSmemLimit - 1024 - BAR_BYTES;
     static constexpr int STAGES_FIT = BUDGET / STAGE_BYTES;
-    static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
+    // An even count: k-tile j uses stage j % STAGES and scale-warp group j % 2, so
+    // every use of a stage belongs to the same group (see the scale warps).
+    static constexpr int STAGES = (STAGES_FIT > 8 ? 8 : STAGES_FIT) & ~1;
     static constexpr int SLOTS = STAGES;
     static constexpr int ACC_BUFS = BN <= 128 ? 2 : 1;
-    static constexpr bool WAITER_COPIES = !MX;   // who issues the scale copies (see the waiter warp)
     static constexpr int SF_COLS = 4 * APK * (1 + NRB);        // TMEM columns of one k-tile's scales
     static constexpr int SF_TMEM = ACC_BUFS * BN;               // first scale column
     static constexpr int TMEM_USED = ACC_BUFS * BN + SLOTS * SF_COLS;
@@ -176,18 +191,23 @@ struct Cfg {
     static constexpr int OFF_B = OFF_A + SLOTS * A_BYTES;
     static constexpr int OFF_SFA = OFF_B + SLOTS * B_BYTES;
     static constexpr int OFF_SFB = OFF_SFA + SLOTS * SFA_BYTES;
-    static constexpr int OFF_STG = OFF_SFB + SLOTS * SFB_BYTES;
-    static constexpr int OFF_BAR = OFF_STG + STAGING_BYTES;
+    static constexpr int OFF_BAR = OFF_SFB + SLOTS * SFB_BYTES;
     static constexpr int SMEM_BYTES = OFF_BAR + BAR_BYTES + 1024;   // + alignment slack
     static constexpr int COLS_WARP = BN / 2;                        // accumulator columns per epilogue warp
-    static constexpr uint32_t TX_BYTES = CG * STAGE_BYTES;          // bytes landing per stage (both CTAs)
+    // The epilogue drains a warp's columns in one pass (its kEpiRegs registers
+    // hold them all) and hands the accumulator back right after.
+    static constexpr int PASSES = 1;
+    static constexpr int PASS_COLS = COLS_WARP / PASSES;
+    static constexpr uint32_t OPND_TX = CG * (A_BYTES + B_BYTES);   // operand bytes landing per stage (both CTAs)
+    static constexpr uint32_t SF_TX = SFA_BYTES + SFB_BYTES;        // scale bytes landing per stage (this CTA)
     static_assert(CG == 1 || CG == 2, "CTA group of 1 or 2");
     static_assert(CG == 1 || BN >= 128, "paired CTAs use N tiles of 128 or 256");
-    static_assert(STAGES >= 2, "too few pipeline stages");
-    static_assert(24 * STAGES + 56 <= BAR_BYTES, "barriers, flags and the scale-copy barriers fit");
+    static_assert(STAGES >= 2 && STAGES % 2 == 0, "an even number of pipeline stages");
+    static_assert(32 * STAGES + 56 <= BAR_BYTES, "barriers and flags fit");
     static_assert(TMEM_USED <= 512, "TMEM budget exceeded");
     static_assert(SMEM_BYTES <= kSmemLimit, "shared memory budget exceeded");
     static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N must be a multiple of 16 in [16, 256]");
+    static_assert(SF_COLS % 8 == 0, "scale columns go out in stores of 8 or 16");
 };
 
 // Records the first error of this device (later ones are dropped).
@@ -199,17 +219,19 @@ __device__ __forceinline__ void record_error(int code)
 // Slow path of wait(): polls with a time bound. On expiry it records
 // FP4_ERR_TIMEOUT in the device status word, raises this CTA's abort flag and
 // returns false; it also gives up once another role of the CTA raised the flag.
-__device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, uint64_t limit_ns,
+// The teardown waits (for a CTA's own copies and MMAs in flight) pass no flag:
+// they end only when the work lands or the time bound runs out.
+__device__ __forceinline__ bool wait_slow(uint32_t bar, uint32_t parity, uint64_t limit_ns,
                                        volatile uint32_t *abort_flag)
 {
     const uint64_t t0 = global_timer_ns();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((it & 255u) == 0) {
-            if (*abort_flag != 0) return false;
+            if (abort_flag && *abort_flag != 0) return false;
             if (global_timer_ns() - t0 > limit_ns) {
                 record_error(FP4_ERR_TIMEOUT);
-                *abort_flag = 1;
+                if (abort_flag) *abort_flag = 1;
                 return false;
             }
         }
@@ -224,7 +246,7 @@ __device__ __forceinline__ bool wait(uint32_t bar, uint32_t parity, uint64_t lim
 }
 
 // Acquire-wait (cluster scope) for barriers that the peer CTA of a pair arrives on.
-__device__ __noinline__ bool wait_cluster_slow(uint32_t bar, uint32_t parity, uint64_t limit_ns,
+__device__ __forceinline__ bool wait_cluster_slow(uint32_t bar, uint32_t parity, uint64_t limit_ns,
                                                volatile uint32_t *abort_flag)
 {
     const uint64_t t0 = global_timer_ns();
@@ -248,31 +270,9 @@ __device__ __forceinline__ bool wait_cluster(uint32_t bar, uint32_t parity, uint
     return wait_cluster_slow(bar, parity, limit_ns, abort_flag);
 }
 
-// MMA thread: waits (bounded) until the waiter's count passes `consumed` and
-// returns it (0 when the wait gave up); the count read with acquire semantics
-// orders the stage's landing (and the accumulator's draining) before the MMAs
-// that follow.
-__device__ __noinline__ uint32_t take_credit(uint32_t ready_addr, uint32_t consumed, uint64_t limit_ns,
-                                             volatile uint32_t *abort_flag)
-{
-    const uint64_t t0 = global_timer_ns();
-    for (uint32_t it = 1;; ++it) {
-        const uint32_t ready = ld_acquire_shared(ready_addr);
-        if (ready > consumed) return ready;
-        if ((it & 63u) == 0) {
-            if (*abort_flag != 0) return 0;
-            if (global_timer_ns() - t0 > limit_ns) {
-                record_error(FP4_ERR_TIMEOUT);
-                *abort_flag = 1;
-                return 0;
-            }
-        }
-    }
-}
-
 // Bounded wait until *flag == epoch (acquire, GPU scope): the first half of a
 // split tail tile has left its partial.
-__device__ __noinline__ bool wait_flag(const unsigned long long *flag, unsigned long long epoch, uint64_t limit_ns,
+__device__ __forceinline__ bool wait_flag(const unsigned long long *flag, unsigned long long epoch, uint64_t limit_ns,
                                        volatile uint32_t *abort_flag)
 {
     const uint64_t t0 = global_timer_ns();
@@ -392,29 +392,192 @@ __device__ __forceinline__ void tmem_load_cols(uint32_t taddr, uint32_t *v)
     }
 }
 
-// One warp stores a 32-row x 32-byte chunk of D: lane l holds row row0 + l's
-// 32 bytes in w[]; they go through the warp's 1 KB staging (16-byte halves
-// swapped on every 4th row against bank conflicts) so that each store
-// instruction writes 16 rows x 32 bytes, i.e. whole sectors. `half_cols` is the
-// element count of 16 bytes.
-__device__ __forceinline__ void store_chunk32(uint8_t *stg, const uint32_t (&w)[8], void *out, int64_t ldo,
-                                              int esize, int row0, int col0, int half_cols, int rows, int cols,
-                                              int lane, uint64_t policy)
+// One thread's 32-byte piece of its D row (w[0..8) = the bytes of columns col ..
+// col + 2 * half_cols - 1): a single 256-bit store when the piece is whole and
+// 32-byte aligned (`whole32`), else two 16-byte halves, each kept to the matrix.
+// A warp's 32 lanes hold 32 rows, so one store instruction writes 32 whole
+// sectors, straight from registers.
+__device__ __forceinline__ void store_row32(const uint32_t (&w)[8], void *out, int64_t ldo, int esize, int row,
+                                            int col, int half_cols, int rows, int cols, bool whole32,
+                                            uint64_t policy)
 {
-    const int sw = (lane >> 2) & 1;
-    *reinterpret_cast<uint4 *>(stg + lane * 32 + (sw << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
-    *reinterpret_cast<uint4 *>(stg + lane * 32 + ((sw ^ 1) << 4)) = make_uint4(w[4], w[5], w[6], w[7]);
-    __syncwarp();
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-        const int piece = 32 * i + lane;
-        const int r = piece >> 1, half = piece & 1;
-        const int row = row0 + r, col = col0 + half * half_cols;
-        const uint4 val = *reinterpret_cast<const uint4 *>(stg + r * 32 + ((half ^ ((r >> 2) & 1)) << 4));
-        if (row < rows && col < cols)
-            st_global_v4_hint(static_cast<char *>(out) + (static_cast<int64_t>(row) * ldo + col) * esize, val, policy);
+    if (row >= rows || col >= cols) return;
+    char *p = static_cast<char *>(out) + (static_cast<int64_t>(row) * ldo + col) * esize;
+    if (whole32 && col + 2 * half_cols <= cols) {
+        st_global_v8_hint(p, w, policy);
+        return;
     }
+    st_global_v4_hint(p, make_uint4(w[0], w[1], w[2], w[3]), policy);
+    if (col + half_cols < cols)
+        st_global_v4_hint(p + 16, make_uint4(w[4], w[5], w[6], w[7]), policy);
+}
+
+// Advances a (stage, phase) ring position.
+template <int STAGES>
+__device__ __forceinline__ void ring_next(int &stage, uint32_t &phase)
+{
+    if (++stage == STAGES) {
+        stage = 0;
+        phase ^= 1u;
+    }
+}
+
+// One epilogue pass: v holds this warp's 32 TMEM lanes x PC accumulator columns,
+// tile columns c0 .. c0 + PC - 1 (slot-B rows tg.tb * BN + c0 ...). Split tail:
+// a first half parks its fp32 partial (column-major, so a fixed column is 32
+// consecutive floats) and, after its last pass, raises its flag; the second
+// half's matching warp waits for the flag once (first pass) and adds it. Then
+// z = alpha * acc + bias, the activation, the cast and the stores.
+template <int CG, int BN, int PC>
+__device__ __forceinline__ void epilogue_pass(uint32_t (&v)[PC], const Args &args, const TileGeo &tg, int c0, int q,
+                                              int lane, int ewarp, uint32_t rank, int split, int half, int tidx,
+                                              bool first_pass, bool last_pass, bool &tail_ok, uint64_t d_policy,
+                                              volatile uint32_t *abort_flag)
+{
+    if (CG == 1 && half >= 0) {   // (pairs never split their last wave)
+        const int slot = tidx * CG + static_cast<int>(rank);
+        float *part = args.tail_ws + (static_cast<int64_t>(slot) * BN + c0) * kBM + 32 * q + lane;
+        unsigned long long *flag = args.tail_flags + slot * kEpiWarps + ewarp;
+        if (half == 0) {
+#pragma unroll
+            for (int i = 0; i < PC; ++i) __stcg(part + i * kBM, __uint_as_float(v[i]));
+            if (last_pass) {
+                __threadfence();
+                __syncwarp();
+                if (lane == 0) st_release_gpu_u64(flag, args.epoch);
+            }
+            return;
+        }
+        if (first_pass) {
+            bool ok = true;
+            if (lane == 0) ok = wait_flag(flag, args.epoch, args.wait_ns, abort_flag);
+            tail_ok = __shfl_sync(0xFFFFFFFFu, ok, 0) && ld_acquire_gpu_u64(flag) == args.epoch;
+        }
+        if (tail_ok) {
+#pragma unroll
+            for (int i = 0; i < PC; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) + __ldcg(part + i * kBM));
+        }
+    }
+    // local rows of the tile's problem (the group's, when grouped)
+    const int row_base = (tg.ta * CG + static_cast<int>(rank)) * kBM + 32 * q;  // this warp's first row
+    const int ra = row_base + lane;                                               // slot-A row of this lane
+    const int col0 = tg.tb * BN + c0;                                             // first slot-B row
+    const bool glu = args.act == FP4_ACT_SWIGLU;
+    if (args.mode != kEpiSplitK) {
+        // z = alpha * acc + bias, then the activation. Rows mode: v[i] is GEMM
+        // column col0 + i; transposed: every v[i] of this lane is GEMM column ra.
+        if (args.bias) {
+            const float *bias = args.bias + tg.bias_off;
+            if (args.mode == kEpiRows) {
+#pragma unroll
+                for (int i = 0; i < PC; ++i) {
+                    const float b = col0 + i < tg.lb ? __ldg(bias + col0 + i) : 0.0f;
+                    v[i] = __float_as_uint(fmaf(__uint_as_float(v[i]), args.alpha, b));
+                }
+            } else {
+                const float b = ra < tg.la ? __ldg(bias + ra) : 0.0f;
+#pragma unroll
+                for (int i = 0; i < PC; ++i) v[i] = __float_as_uint(fmaf(__uint_as_float(v[i]), args.alpha, b));
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < PC; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * args.alpha);
+        }
+        if (glu) {
+            if (args.mode == kEpiRows) {
+                // gate = even column, up = odd column: pack the PC/2 results into v[0 .. PC/2)
+#pragma unroll
+                for (int j = 0; j < PC / 2; ++j)
+                    v[j] = __float_as_uint(silu(__uint_as_float(v[2 * j])) * __uint_as_float(v[2 * j + 1]));
+            } else {
+                // gate on the even lane, up on the odd lane next to it
+#pragma unroll
+                for (int i = 0; i < PC; ++i) {
+                    const float z = __uint_as_float(v[i]);
+                    const float up = __shfl_xor_sync(0xFFFFFFFFu, z, 1);
+                    v[i] = __float_as_uint(silu(z) * up);
+                }
+            }
+        } else if (args.act != FP4_ACT_NONE) {
+#pragma unroll
+            for (int i = 0; i < PC; ++i) v[i] = __float_as_uint(activate(__uint_as_float(v[i]), args.act));
+        }
+    }
+    if (args.mode == kEpiRows) {
+        // this lane's D row in 32-byte column pieces; SwiGLU stores half as many
+        // columns, from D column col0 / 2
+        const int oc0 = glu ? col0 >> 1 : col0;
+        const int ocols = glu ? tg.lb >> 1 : tg.lb;
+        const int nval = glu ? PC / 2 : PC;
+        if (args.bf16) {
+#pragma unroll
+            for (int ch = 0; ch < PC / 16; ++ch) {
+                if (16 * ch < nval) {
+                    uint32_t w[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        __nv_bfloat162 p = __floats2bfloat162_rn(__uint_as_float(v[16 * ch + 2 * i]),
+                                                                 __uint_as_float(v[16 * ch + 2 * i + 1]));
+                        w[i] = *reinterpret_cast<uint32_t *>(&p);
+                    }
+                    store_row32(w, args.out, args.ldo, 2, tg.da + ra, oc0 + 16 * ch, 8, tg.da + tg.la, ocols,
+                                args.st32, d_policy);
+                }
+            }
+        } else {
+#pragma unroll
+            for (int ch = 0; ch < PC / 8; ++ch) {
+                if (8 * ch < nval) {
+                    uint32_t w[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) w[i] = v[8 * ch + i];
+                    store_row32(w, args.out, args.ldo, 4, tg.da + ra, oc0 + 8 * ch, 4, tg.da + tg.la, ocols,
+                                args.st32, d_policy);
+                }
+            }
+        }
+    } else if (ra < tg.la) {
+        if (args.mode == kEpiSplitK) {
+            // fp32 partials, transposed: for a fixed column the 32 lanes of a warp
+            // write 32 consecutive elements
+            float *ws = static_cast<float *>(args.out) + split * args.split_stride + ra;
+#pragma unroll
+            for (int i = 0; i < PC; ++i)
+                if (col0 + i < args.rows_b)
+                    st_global_b32_hint(ws + static_cast<int64_t>(col0 + i) * args.ldo, v[i], d_policy);
+        } else if (!glu || (lane & 1) == 0) {
+            // D^T: this lane's GEMM column ra (SwiGLU: D column ra / 2, from the gate
+            // lane); D row db + (slot-B row)
+            const int oc = tg.da + (glu ? ra >> 1 : ra);
+            const int r0 = tg.db + col0;
+            if (args.bf16) {
+                __nv_bfloat16 *d = static_cast<__nv_bfloat16 *>(args.out) + oc;
+#pragma unroll
+                for (int i = 0; i < PC; ++i)
+                    if (col0 + i < tg.lb)
+                        st_global_b16_hint(d + static_cast<int64_t>(r0 + i) * args.ldo,
+                                           __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v[i]))), d_policy);
+            } else {
+                float *d = static_cast<float *>(args.out) + oc;
+#pragma unroll
+                for (int i = 0; i < PC; ++i)
+                    if (col0 + i < tg.lb) st_global_b32_hint(d + static_cast<int64_t>(r0 + i) * args.ldo, v[i], d_policy);
+            }
+        }
+    }
+}
+
+// End of a warp role: all of the block (and of the pair) meets once every
+// role's work, with its copies, MMAs and TMEM accesses, is done. Each role
+// branch has its own copy (the branches run with different register counts, so
+// no code may follow them in common).
+template <int CG>
+__device__ __forceinline__ void role_end()
+{
     __syncwarp();
+    tc_fence_before();
+    if constexpr (CG == 2) cluster_sync_any(); else cta_sync_any();
+    tc_fence_after();
 }
 
 template <int CG, int BN, bool MX, bool GROUPED>
@@ -428,17 +591,20 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tmap_a, const CUten
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t *const base_ptr = smem_raw + (base - raw);
 
+    // Barriers, per stage s: full (the leader's: both CTAs' operand tiles landed),
+    // full_sf (this CTA's scale atoms landed), empty (the stage's MMAs completed;
+    // the leader's commit reaches both CTAs), sf_ready (the leader's: both CTAs'
+    // scale warps have stored the stage's scales in TMEM).
     const uint32_t bar_full = base + C::OFF_BAR;
-    const uint32_t bar_empty = bar_full + 8 * C::STAGES;
-    const uint32_t bar_acc_full = bar_empty + 8 * C::STAGES;
+    const uint32_t bar_full_sf = bar_full + 8 * C::STAGES;
+    const uint32_t bar_empty = bar_full_sf + 8 * C::STAGES;
+    const uint32_t bar_sf_ready = bar_empty + 8 * C::STAGES;
+    const uint32_t bar_acc_full = bar_sf_ready + 8 * C::STAGES;
     const uint32_t bar_acc_empty = bar_acc_full + 16;
     const uint32_t bar_drain = bar_acc_empty + 16;
-    uint32_t *const tmem_holder = reinterpret_cast<uint32_t *>(base_ptr + C::OFF_BAR + 16 * C::STAGES + 40);
+    uint32_t *const tmem_holder = reinterpret_cast<uint32_t *>(base_ptr + C::OFF_BAR + 32 * C::STAGES + 40);
     volatile uint32_t *const abort_flag =
-        reinterpret_cast<volatile uint32_t *>(base_ptr + C::OFF_BAR + 16 * C::STAGES + 44);
-    // stages the waiter warp has seen land (a count, in the MMA issue order)
-    const uint32_t ready_addr = base + C::OFF_BAR + 16 * C::STAGES + 48;
-    const uint32_t bar_sf = base + C::OFF_BAR + 16 * C::STAGES + 56;     // scale copies of stage s done
+        reinterpret_cast<volatile uint32_t *>(base_ptr + C::OFF_BAR + 32 * C::STAGES + 44);
 
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
@@ -449,16 +615,16 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tmap_a, const CUten
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::STAGES; ++s) {
             mbar_init(bar_full + 8 * s, 1);
+            mbar_init(bar_full_sf + 8 * s, 1);
             mbar_init(bar_empty + 8 * s, 1);
+            mbar_init(bar_sf_ready + 8 * s, (kSfWarps / 2) * CG);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(bar_acc_full + 8 * b, 1);
             mbar_init(bar_acc_empty + 8 * b, kEpiWarps * CG);
         }
         mbar_init(bar_drain, 1);
-        for (int st = 0; st < C::STAGES; ++st) mbar_init(bar_sf + 8 * st, 1);
         *abort_flag = 0;
-        st_release_shared(ready_addr, 0);
         fence_mbarrier_init();
     }
     if (threadIdx.x == 32) {
@@ -479,15 +645,21 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tmap_a, const CUten
     // its tail; nothing in memory is touched before it has completed.
     griddep_wait();
 
+    // Roles by warpgroup; each warpgroup's register split comes first in its own
+    // branch, so the code after it is compiled for that many registers.
+    if (warp < kFirstEpiWarp) {
+        regs_lower<kLowRegs>();
     if (warp == 0) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
-            // every CTA signals the leader's full barrier; the leader posts the
-            // byte count of both CTAs
+            // every CTA's operand tiles signal the leader's full barrier (the leader
+            // posts the byte count of both CTAs); its scale atoms signal its own
+            // full_sf barrier
             const uint32_t full0 = CG == 2 ? mapa_shared(bar_full, 0) : bar_full;
             int stage = 0;
             uint32_t phase = 0;
             uint32_t filled = 0, fill_parity = 0;
+            uint32_t pfilled = 0;                 // stages this producer has filled
             bool ok = true;
             for (int u = pair; ok && u < args.units; u += npairs) {
                 int ta, tb, split, kt0, kt1, half, tidx;
@@ -500,35 +672,43 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tmap_a, const CUten
                 const int sba = tg.sa + rba;                             // its scale block
                 const int rbb = tg.sb + (tg.tb * BN) / 128;              // first scale block of the N side
                 for (int kt = kt0; kt < kt1; ++kt) {
+                    if (args.stop_after > 0 && pfilled >= static_cast<uint32_t>(args.stop_after)) {
+                        ok = false;     // (bounded-wait test: this stage is never loaded)
+                        break;
+                    }
                     if (!wait(bar_empty + 8 * stage, phase ^ 1u, args.wait_ns, abort_flag)) {
                         ok = false;
                         break;
                     }
+                    ++pfilled;
                     const uint32_t full = full0 + 8 * stage;                 // shared::cluster address
-                    if (rank == 0) mbar_arrive_expect_tx(bar_full + 8 * stage, C::TX_BYTES);
-                    const int slot = stage;
-                    tma_load_2d<CG>(base + C::OFF_A + slot * C::A_BYTES, &tmap_a, full, kt * kBKBytes, row_a);
-                    tma_load_2d<CG>(base + C::OFF_B + slot * C::B_BYTES, &tmap_b, full, kt * kBKBytes, row_b);
-                    tma_load_2d<CG>(base + C::OFF_SFA + slot * C::SFA_BYTES, &tmap_sfa, full,
-                                    kt * C::APK * (kAtomBytes / 8), sba);
-                    tma_load_2d<CG>(base + C::OFF_SFB + slot * C::SFB_BYTES, &tmap_sfb, full,
-                                    kt * C::APK * (kAtomBytes / 8), rbb);
+                    const uint32_t full_sf = bar_full_sf + 8 * stage;
+                    if (rank == 0) mbar_arrive_expect_tx(bar_full + 8 * stage, C::OPND_TX);
+                    mbar_arrive_expect_tx(full_sf, C::SF_TX);
+                    tma_load_2d<CG>(base + C::OFF_A + stage * C::A_BYTES, &tmap_a, full, kt * kBKBytes, row_a);
+                    tma_load_2d<CG>(base + C::OFF_B + stage * C::B_BYTES, &tmap_b, full, kt * kBKBytes, row_b);
+                    tma_load_2d<1>(base + C::OFF_SFA + stage * C::SFA_BYTES, &tmap_sfa, full_sf,
+                                   kt * C::APK * (kAtomBytes / 8), sba);
+                    tma_load_2d<1>(base + C::OFF_SFB + stage * C::SFB_BYTES, &tmap_sfb, full_sf,
+                                   kt * C::APK * (kAtomBytes / 8), rbb);
                     filled |= 1u << stage;
                     fill_parity = (fill_parity & ~(1u << stage)) | (phase << stage);
-                    if (++stage == C::STAGES) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
+                    ring_next<C::STAGES>(stage, phase);
                 }
             }
-            // The leader lets every copy it waited for land before the CTA can exit;
-            // the peer's copies signal the leader, whose MMA warp waits for them.
-            if (rank == 0)
-                for (int s = 0; s < C::STAGES; ++s)
-                    if (filled & (1u << s)) wait(bar_full + 8 * s, (fill_parity >> s) & 1u, args.wait_ns, abort_flag);
+            // Every copy this CTA issued lands before it can exit: its scale atoms on
+            // its own barriers, both CTAs' operand tiles on the leader's.
+            for (int s = 0; s < C::STAGES; ++s)
+                if (filled & (1u << s)) {
+                    wait(bar_full_sf + 8 * s, (fill_parity >> s) & 1u, args.wait_ns, nullptr);
+                    if (rank == 0) wait(bar_full + 8 * s, (fill_parity >> s) & 1u, args.wait_ns, nullptr);
+                }
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
+        // This thread issues only MMAs and commits (the scale warps stage the
+        // scales): with no tcgen05.cp of its own outstanding, its per-stage
+        // mbarrier waits cost nothing on the tensor pipe.
         if (lane == 0 && rank == 0) {
             // Instruction descriptors: MXFP4 alternates the scale byte ids 0 / 2
             // between the two K=64 halves of one 4-block atom.
@@ -538,13 +718,10 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tmap_a, const CUten
             // apart; MMA j of a k-tile starts 32 bytes (two 16-byte units) in.
             const uint64_t desc_a0 = smem_desc(base + C::OFF_A, 16, 1024, 2);
             const uint64_t desc_b0 = smem_desc(base + C::OFF_B, 16, 1024, 2);
-            // scale atom: 32 rows of 16 bytes, 8-row groups 128 bytes apart
-            const uint64_t desc_sfa0 = smem_desc(base + C::OFF_SFA, 0, 128, 0);
-            const uint64_t desc_sfb0 = smem_desc(base + C::OFF_SFB, 0, 128, 0);
             int stage = 0;
+            uint32_t phase = 0;
             int acc = 0;
             uint32_t acc_phase = 0;
-            uint32_t consumed = 0, ready = 0;    // stages issued / stages known to have landed
             bool ok = true;
             for (int u = pair; ok && u < args.units; u += npairs) {
                 int ta, tb, split, kt0, kt1, half, tidx;
@@ -553,43 +730,26 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tmap_a, const CUten
                 if (!wait_cluster(bar_acc_empty + 8 * acc, acc_phase ^ 1u, args.wait_ns, abort_flag)) break;
                 const uint32_t d_tmem = tmem + static_cast<uint32_t>(acc * BN);
                 for (int kt = kt0; kt < kt1; ++kt) {
-                    // The waiter warp has seen this stage land once its count passes `consumed`.
-                    if (ready == consumed) {
-                        ready = take_credit(ready_addr, consumed, args.wait_ns, abort_flag);
-                        if (ready == 0) {
-                            ok = false;
-                            break;
-                        }
+                    // the stage's operands (both CTAs) and scales (both CTAs' TMEM) are in place
+                    if (!wait(bar_full + 8 * stage, phase, args.wait_ns, abort_flag) ||
+                        !wait_cluster(bar_sf_ready + 8 * stage, phase, args.wait_ns, abort_flag)) {
+                        ok = false;
+                        break;
                     }
                     tc_fence_after();
-                    {
-                        const int slot = stage;
-                        const uint32_t sf = tmem + static_cast<uint32_t>(C::SF_TMEM + slot * C::SF_COLS);
-                        if constexpr (!C::WAITER_COPIES) {
-                            const uint64_t dsa = desc_sfa0 + static_cast<uint64_t>((slot * C::SFA_BYTES) >> 4);
-                            const uint64_t dsb = desc_sfb0 + static_cast<uint64_t>((slot * C::SFB_BYTES) >> 4);
+                    const uint32_t sf = tmem + static_cast<uint32_t>(C::SF_TMEM + stage * C::SF_COLS);
+                    const uint64_t da = desc_a0 + static_cast<uint64_t>((stage * C::A_BYTES) >> 4);
+                    const uint64_t db = desc_b0 + static_cast<uint64_t>((stage * C::B_BYTES) >> 4);
 #pragma unroll
-                            for (int t = 0; t < C::APK; ++t) {
-                                tc_cp_32x128b_warpx4<CG>(sf + 4 * t, dsa + (t * kAtomBytes >> 4));
-#pragma unroll
-                                for (int rb = 0; rb < C::NRB; ++rb)
-                                    tc_cp_32x128b_warpx4<CG>(sf + 4 * C::APK + 4 * (t * C::NRB + rb),
-                                                             dsb + ((rb * C::APK + t) * kAtomBytes >> 4));
-                            }
-                        }
-                        const uint64_t da = desc_a0 + static_cast<uint64_t>((slot * C::A_BYTES) >> 4);
-                        const uint64_t db = desc_b0 + static_cast<uint64_t>((slot * C::B_BYTES) >> 4);
-#pragma unroll
-                        for (int i = 0; i < kBK / 64; ++i) {
-                            const int t = MX ? (i >> 1) : i;
-                            const uint32_t idesc = (MX && (i & 1)) ? ID2 : ID0;
-                            tc_mma_fp4<CG, MX>(d_tmem, da + 2 * i, db + 2 * i, idesc, sf + 4 * t,
-                                               sf + 4 * C::APK + 4 * C::NRB * t, (kt > kt0 || i > 0) ? 1u : 0u);
-                        }
+                    for (int i = 0; i < kBK / 64; ++i) {
+                        const int t = MX ? (i >> 1) : i;
+                        const uint32_t idesc = (MX && (i & 1)) ? ID2 : ID0;
+                        tc_mma_fp4<CG, MX>(d_tmem, da + 2 * i, db + 2 * i, idesc, sf + 4 * t,
+                                           sf + 4 * C::APK + 4 * C::NRB * t, (kt > kt0 || i > 0) ? 1u : 0u);
                     }
+                    // frees the stage: its shared memory and its TMEM scale columns
                     tc_commit<CG>(bar_empty + 8 * stage);
-                    ++consumed;
-                    if (++stage == C::STAGES) stage = 0;
+                    ring_next<C::STAGES>(stage, phase);
                 }
                 if (!ok) break;
                 tc_commit<CG>(bar_acc_full + 8 * acc);
@@ -600,74 +760,98 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tmap_a, const CUten
                     acc_phase ^= 1u;
                 }
             }
-            // Every MMA and scale copy this thread issued completes before teardown.
+            // Every MMA this thread issued completes before teardown.
             tc_commit<CG>(bar_drain, 1);
-            wait(bar_drain, 0, args.wait_ns, abort_flag);
+            wait(bar_drain, 0, args.wait_ns, nullptr);
         }
-    } else if (warp == kWaiterWarp) {
-        // ------------------------------------------------------------ waiter
-        // Waits, in the MMA issue order, for each stage to land and publishes
-        // the running count, so that the MMA thread blocks in an mbarrier wait
-        // only once per tile (for the accumulator): on this part a wait in the
-        // issuing thread costs about 200 cycles in which the tensor core runs
-        // dry. For NVFP4 (twelve scale copies per k-tile) it also copies the
-        // stage's scale atoms into the stage's TMEM slot (tcgen05.cp) and waits
-        // for them before publishing, so that the copies overlap the MMAs of
-        // earlier stages instead of queueing behind them in the MMA thread (one
-        // CTA per MMA: 4096^3 55.4 -> 51.4 us, 8192 x 4096 x 14336 262 -> 236 us;
-        // CTA pairs: 8192^3 313 -> 299 us). MXFP4 (six copies per k-tile) keeps
-        // them in the MMA thread: there the split measured slower (8192^3 with
-        // CTA pairs 231 -> 287 us, with one CTA per MMA 250 -> 274 us).
-        if (lane == 0 && rank == 0) {
-            // scale atom: 32 rows of 16 bytes, 8-row groups 128 bytes apart
-            const uint64_t desc_sfa0 = smem_desc(base + C::OFF_SFA, 0, 128, 0);
-            const uint64_t desc_sfb0 = smem_desc(base + C::OFF_SFB, 0, 128, 0);
-            int stage = 0;
-            uint32_t phase = 0;
-            uint32_t seen = 0;
-            bool ok = true;
-            for (int u = pair; ok && u < args.units; u += npairs) {
-                int ta, tb, split, kt0, kt1, half, tidx;
-                unit_work<GROUPED>(args, u, ta, tb, split, kt0, kt1, half, tidx);
-                for (int kt = kt0; kt < kt1; ++kt) {
-                    if (!wait(bar_full + 8 * stage, phase, args.wait_ns, abort_flag)) {
+    }
+        role_end<CG>();
+        if (warp == 1) tmem_dealloc<CG>(tmem, C::TMEM_COLS);
+    } else if (warp >= kFirstSfWarp) {
+        regs_lower<kLowRegs>();
+        // ------------------------------------------------------------ scale warps
+        // Each TMEM lane quarter q has two scale warps, taking alternate k-tiles.
+        // For a k-tile, the warp reads its lane's line of every scale atom of the
+        // stage (16 bytes each) and stores them in this quarter's lanes of the
+        // stage's TMEM scale columns with tcgen05.st: column 4t + c of slot A holds
+        // line i, word c of atom t (the scales of row 32c + i, K-chunk t); slot B
+        // likewise per 128-row block. The MMA reads, in quarter q, column q of
+        // each slot-A group and every slot-B column, so every quarter gets the
+        // same bytes. (Copying the atoms with tcgen05.cp instead, beside the
+        // MMAs, measured 1.5-2.5x slower per k-tile on this part.)
+        const int q = warp & 3;
+        const int grp = (warp - kFirstSfWarp) >> 2;
+        const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
+        const uint32_t ready0 = CG == 2 ? mapa_shared(bar_sf_ready, 0) : bar_sf_ready;
+        int stage = 0;
+        uint32_t phase = 0;
+        uint32_t seq = 0;
+        bool ok = true;
+        for (int u = pair; ok && u < args.units; u += npairs) {
+            int ta, tb, split, kt0, kt1, half, tidx;
+            unit_work<GROUPED>(args, u, ta, tb, split, kt0, kt1, half, tidx);
+            for (int kt = kt0; kt < kt1; ++kt, ++seq) {
+                // A group takes every other k-tile; with an even stage count those
+                // always use the group's own stages, so the group waits on every phase
+                // of exactly the barriers it helps complete, in order: a parity wait
+                // is only sound when the waiter has seen the barrier's previous phase
+                // and the next one cannot complete without it.
+                if (static_cast<int>(seq & 1u) == grp) {
+                    // this CTA's scale atoms of the stage have landed (which also means
+                    // the MMAs that read the slot's previous scales have completed)
+                    bool landed = true;
+                    if (lane == 0) landed = wait(bar_full_sf + 8 * stage, phase, args.wait_ns, abort_flag);
+                    if (!__shfl_sync(0xFFFFFFFFu, landed, 0)) {
                         ok = false;
                         break;
                     }
-                    if constexpr (C::WAITER_COPIES) {
-                        tc_fence_after();
-                        const uint32_t sf = tmem + static_cast<uint32_t>(C::SF_TMEM + stage * C::SF_COLS);
-                        const uint64_t dsa = desc_sfa0 + static_cast<uint64_t>((stage * C::SFA_BYTES) >> 4);
-                        const uint64_t dsb = desc_sfb0 + static_cast<uint64_t>((stage * C::SFB_BYTES) >> 4);
+                    tc_fence_after();
+                    // 16 columns (four atoms) at a time: group g of four columns is
+                    // slot-A atom g (g < APK), else slot-B atom (t, rb) with
+                    // g - APK = t * NRB + rb
+                    const uint32_t col = lane_base + tmem + static_cast<uint32_t>(C::SF_TMEM + stage * C::SF_COLS);
+                    const uint8_t *sfa = base_ptr + C::OFF_SFA + stage * C::SFA_BYTES + lane * 16;
+                    const uint8_t *sfb = base_ptr + C::OFF_SFB + stage * C::SFB_BYTES + lane * 16;
 #pragma unroll
-                        for (int t = 0; t < C::APK; ++t) {
-                            tc_cp_32x128b_warpx4<CG>(sf + 4 * t, dsa + (t * kAtomBytes >> 4));
+                    for (int c0 = 0; c0 < C::SF_COLS; c0 += 16) {
+                        uint32_t r[16];
 #pragma unroll
-                            for (int rb = 0; rb < C::NRB; ++rb)
-                                tc_cp_32x128b_warpx4<CG>(sf + 4 * C::APK + 4 * (t * C::NRB + rb),
-                                                         dsb + ((rb * C::APK + t) * kAtomBytes >> 4));
+                        for (int a = 0; a < 4; ++a) {
+                            const int g = c0 / 4 + a;
+                            if (4 * g < C::SF_COLS) {
+                                const uint8_t *src = g < C::APK ? sfa + g * kAtomBytes
+                                                                : sfb + (((g - C::APK) % C::NRB) * C::APK +
+                                                                         (g - C::APK) / C::NRB) * kAtomBytes;
+                                const uint4 w = *reinterpret_cast<const uint4 *>(src);
+                                r[4 * a] = w.x, r[4 * a + 1] = w.y, r[4 * a + 2] = w.z, r[4 * a + 3] = w.w;
+                            }
                         }
-                        tc_commit<CG>(bar_sf + 8 * stage, 1);     // this CTA's barrier only
-                        if (!wait(bar_sf + 8 * stage, phase, args.wait_ns, abort_flag)) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_before();
+                        if (c0 + 16 <= C::SF_COLS)
+                            tmem_st_32x32b_x16(col + c0, r);
+                        else
+                            tmem_st_32x32b_x8(col + c0, r);
                     }
-                    st_release_shared(ready_addr, ++seen);
-                    if (++stage == C::STAGES) {
-                        stage = 0;
-                        phase ^= 1u;
+                    tmem_st_wait();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) {
+                        if constexpr (CG == 2)
+                            mbar_arrive_cluster(ready0 + 8 * stage);
+                        else
+                            mbar_arrive(bar_sf_ready + 8 * stage);
                     }
                 }
+                ring_next<C::STAGES>(stage, phase);
             }
         }
+        role_end<CG>();
     } else {
+        regs_raise<kEpiRegs>();
         // ------------------------------------------------------------ epilogue
         const int q = warp & 3;                          // TMEM lane quarter of this warp
-        const int h = (warp - 2) >> 2;                   // which half of the tile's columns
+        const int ew = warp - kFirstEpiWarp;             // epilogue warp index
+        const int h = ew >> 2;                           // which half of the tile's columns
         const uint32_t acc_empty0 = CG == 2 ? mapa_shared(bar_acc_empty, 0) : bar_acc_empty;
-        uint8_t *const stg_ptr = base_ptr + C::OFF_STG + (warp - 2) * kStgBytes;
         // D is written once and not read again here: evict it from L2 first, so the
         // operand tiles that other CTAs still load stay resident.
         const uint64_t d_policy = policy_evict_first();
@@ -680,162 +864,29 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tmap_a, const CUten
             tile_geo<GROUPED>(args, gp, u, ta, tb, tg);
             if (!wait(bar_acc_full + 8 * acc, acc_phase, args.wait_ns, abort_flag)) break;
             tc_fence_after();
-            // Drain this warp's 32 lanes x BN/2 columns, then release the accumulator.
-            uint32_t v[C::COLS_WARP];
-            tmem_load_cols<C::COLS_WARP>(tmem + (static_cast<uint32_t>(32 * q) << 16) +
-                                             static_cast<uint32_t>(acc * BN + h * C::COLS_WARP),
-                                         v);
-            tmem_ld_wait_regs(v);
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) {
-                if constexpr (CG == 2)
-                    mbar_arrive_cluster(acc_empty0 + 8 * acc);
-                else
-                    mbar_arrive(bar_acc_empty + 8 * acc);
-            }
-            // Split tail: a first half parks its fp32 partial (this warp's 32 rows x
-            // BN/2 columns, column-major so a fixed column is 32 consecutive floats)
-            // and raises its flag; the second half's matching warp adds it.
-            bool store_d = true;
-            if (CG == 1 && half >= 0) {   // (pairs never split: their epilogue has no registers to spare)
-                const int slot = tidx * CG + static_cast<int>(rank);
-                float *part = args.tail_ws + (static_cast<int64_t>(slot) * BN + h * C::COLS_WARP) * kBM + 32 * q + lane;
-                unsigned long long *flag = args.tail_flags + slot * kEpiWarps + (warp - 2);
-                if (half == 0) {
-#pragma unroll
-                    for (int i = 0; i < C::COLS_WARP; ++i) __stcg(part + i * kBM, __uint_as_float(v[i]));
-                    __threadfence();
+            // This warp's 32 lanes x BN/2 columns, in passes; the accumulator is
+            // handed back as soon as the last pass is in registers.
+            bool tail_ok = false;
+#pragma unroll 1
+            for (int p = 0; p < C::PASSES; ++p) {
+                const int c0 = h * C::COLS_WARP + p * C::PASS_COLS;
+                uint32_t v[C::PASS_COLS];
+                tmem_load_cols<C::PASS_COLS>(tmem + (static_cast<uint32_t>(32 * q) << 16) +
+                                                 static_cast<uint32_t>(acc * BN + c0),
+                                             v);
+                tmem_ld_wait_regs(v);
+                if (p == C::PASSES - 1) {
+                    tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) st_release_gpu_u64(flag, args.epoch);
-                    store_d = false;
-                } else {
-                    bool ok = true;
-                    if (lane == 0) ok = wait_flag(flag, args.epoch, args.wait_ns, abort_flag);
-                    ok = __shfl_sync(0xFFFFFFFFu, ok, 0) && ld_acquire_gpu_u64(flag) == args.epoch;
-                    if (ok) {
-#pragma unroll
-                        for (int i = 0; i < C::COLS_WARP; ++i)
-                            v[i] = __float_as_uint(__uint_as_float(v[i]) + __ldcg(part + i * kBM));
+                    if (lane == 0) {
+                        if constexpr (CG == 2)
+                            mbar_arrive_cluster(acc_empty0 + 8 * acc);
+                        else
+                            mbar_arrive(bar_acc_empty + 8 * acc);
                     }
                 }
-            }
-            if (store_d) {
-                // local rows of the tile's problem (the group's, when grouped)
-                const int row_base = (tg.ta * CG + static_cast<int>(rank)) * kBM + 32 * q;  // this warp's first row
-                const int ra = row_base + lane;                                               // slot-A row of this lane
-                const int col0 = tg.tb * BN + h * C::COLS_WARP;                                // first slot-B row
-                const bool glu = args.act == FP4_ACT_SWIGLU;
-                if (args.mode != kEpiSplitK) {
-                    // z = alpha * acc + bias, then the activation. Rows mode: v[i] is
-                    // GEMM column col0 + i; transposed: every v[i] of this lane is
-                    // GEMM column ra.
-                    if (args.bias) {
-                        const float *bias = args.bias + tg.bias_off;
-                        if (args.mode == kEpiRows) {
-#pragma unroll
-                            for (int i = 0; i < C::COLS_WARP; ++i) {
-                                const float b = col0 + i < tg.lb ? __ldg(bias + col0 + i) : 0.0f;
-                                v[i] = __float_as_uint(fmaf(__uint_as_float(v[i]), args.alpha, b));
-                            }
-                        } else {
-                            const float b = ra < tg.la ? __ldg(bias + ra) : 0.0f;
-#pragma unroll
-                            for (int i = 0; i < C::COLS_WARP; ++i)
-                                v[i] = __float_as_uint(fmaf(__uint_as_float(v[i]), args.alpha, b));
-                        }
-                    } else {
-#pragma unroll
-                        for (int i = 0; i < C::COLS_WARP; ++i)
-                            v[i] = __float_as_uint(__uint_as_float(v[i]) * args.alpha);
-                    }
-                    if (glu) {
-                        if (args.mode == kEpiRows) {
-                            // gate = even column, up = odd column: pack the N/2 results
-                            // into v[0 .. COLS_WARP/2)
-#pragma unroll
-                            for (int j = 0; j < C::COLS_WARP / 2; ++j)
-                                v[j] = __float_as_uint(silu(__uint_as_float(v[2 * j])) *
-                                                       __uint_as_float(v[2 * j + 1]));
-                        } else {
-                            // gate on the even lane, up on the odd lane next to it
-#pragma unroll
-                            for (int i = 0; i < C::COLS_WARP; ++i) {
-                                const float z = __uint_as_float(v[i]);
-                                const float up = __shfl_xor_sync(0xFFFFFFFFu, z, 1);
-                                v[i] = __float_as_uint(silu(z) * up);
-                            }
-                        }
-                    } else if (args.act != FP4_ACT_NONE) {
-#pragma unroll
-                        for (int i = 0; i < C::COLS_WARP; ++i)
-                            v[i] = __float_as_uint(activate(__uint_as_float(v[i]), args.act));
-                    }
-                }
-                if (args.mode == kEpiRows || ra < tg.la) {             // the row stores are warp-collective
-                    if (args.mode == kEpiRows) {
-                        // D rows of this warp in 32-byte column chunks through the staging;
-                        // SwiGLU stores half as many columns, from D column col0 / 2
-                        const int oc0 = glu ? col0 >> 1 : col0;
-                        const int ocols = glu ? tg.lb >> 1 : tg.lb;
-                        const int nval = glu ? C::COLS_WARP / 2 : C::COLS_WARP;
-                        if (args.bf16) {
-#pragma unroll
-                            for (int ch = 0; ch < C::COLS_WARP / 16; ++ch) {
-                                if (16 * ch < nval) {
-                                    uint32_t w[8];
-#pragma unroll
-                                    for (int i = 0; i < 8; ++i) {
-                                        __nv_bfloat162 p = __floats2bfloat162_rn(__uint_as_float(v[16 * ch + 2 * i]),
-                                                                                 __uint_as_float(v[16 * ch + 2 * i + 1]));
-                                        w[i] = *reinterpret_cast<uint32_t *>(&p);
-                                    }
-                                    store_chunk32(stg_ptr, w, args.out, args.ldo, 2, tg.da + row_base, oc0 + 16 * ch, 8,
-                                                  tg.da + tg.la, ocols, lane, d_policy);
-                                }
-                            }
-                        } else {
-#pragma unroll
-                            for (int ch = 0; ch < C::COLS_WARP / 8; ++ch) {
-                                if (8 * ch < nval) {
-                                    uint32_t w[8];
-#pragma unroll
-                                    for (int i = 0; i < 8; ++i) w[i] = v[8 * ch + i];
-                                    store_chunk32(stg_ptr, w, args.out, args.ldo, 4, tg.da + row_base, oc0 + 8 * ch, 4,
-                                                  tg.da + tg.la, ocols, lane, d_policy);
-                                }
-                            }
-                        }
-                    } else if (args.mode == kEpiSplitK) {
-                        // fp32 partials, transposed: for a fixed column the 32 lanes of a
-                        // warp write 32 consecutive elements
-                        float *ws = static_cast<float *>(args.out) + split * args.split_stride + ra;
-#pragma unroll
-                        for (int i = 0; i < C::COLS_WARP; ++i)
-                            if (col0 + i < args.rows_b)
-                                st_global_b32_hint(ws + static_cast<int64_t>(col0 + i) * args.ldo, v[i], d_policy);
-                    } else if (!glu || (lane & 1) == 0) {
-                        // D^T: this lane's GEMM column ra (SwiGLU: D column ra / 2, from the gate
-                        // lane); D row db + (slot-B row)
-                        const int oc = tg.da + (glu ? ra >> 1 : ra);
-                        const int r0 = tg.db + col0;
-                        if (args.bf16) {
-                            __nv_bfloat16 *d = static_cast<__nv_bfloat16 *>(args.out) + oc;
-#pragma unroll
-                            for (int i = 0; i < C::COLS_WARP; ++i)
-                                if (col0 + i < tg.lb)
-                                    st_global_b16_hint(d + static_cast<int64_t>(r0 + i) * args.ldo,
-                                                       __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v[i]))),
-                                                       d_policy);
-                        } else {
-                            float *d = static_cast<float *>(args.out) + oc;
-#pragma unroll
-                            for (int i = 0; i < C::COLS_WARP; ++i)
-                                if (col0 + i < tg.lb)
-                                    st_global_b32_hint(d + static_cast<int64_t>(r0 + i) * args.ldo, v[i], d_policy);
-                        }
-                    }
-                }
+                epilogue_pass<CG, BN, C::PASS_COLS>(v, args, tg, c0, q, lane, ew, rank, split, half, tidx, p == 0,
+                                                    p == C::PASSES - 1, tail_ok, d_policy, abort_flag);
             }
             if (C::ACC_BUFS == 2) {
                 acc ^= 1;
@@ -844,13 +895,8 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tmap_a, const CUten
                 acc_phase ^= 1u;
             }
         }
+        role_end<CG>();
     }
-
-    __syncwarp();
-    tc_fence_before();
-    if constexpr (CG == 2) cluster_sync(); else __syncthreads();
-    tc_fence_after();
-    if (warp == 1) tmem_dealloc<CG>(tmem, C::TMEM_COLS);
 }
 
 template <int CG, int BN, bool MX>
@@ -1012,7 +1058,28 @@ namespace {
 
 std::mutex g_mu;
 int64_t g_wait_ms = -1;
-std::atomic<unsigned long long> g_epoch{0};   // per-launch value of the split-tail flags
+std::atomic<unsigned long long> g_epoch{0};   // launches so far (see next_epoch)
+
+// The split-tail flags' value for the next launch. The flags live in scratch
+// that earlier calls (or other code) filled with arbitrary bytes, so a flag
+// counts as raised only when it holds this launch's value: a per-process random
+// 64-bit nonce mixed with the launch counter through a bijective finaliser
+// (SplitMix64's), so two launches of one process never share a value and stale
+// bytes match one with probability 2^-64.
+unsigned long long next_epoch()
+{
+    static const unsigned long long nonce = [] {
+        std::random_device rd;
+        unsigned long long n = (static_cast<unsigned long long>(rd()) << 32) ^ rd();
+        n ^= static_cast<unsigned long long>(std::chrono::steady_clock::now().time_since_epoch().count());
+        return n;
+    }();
+    unsigned long long z = nonce + 0x9E3779B97F4A7C15ull * ++g_epoch;
+    z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+    z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+    z ^= z >> 31;
+    return z ? z : 1ull;
+}
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
 // True when work issued to `stream` is being recorded into a CUDA graph (or
@@ -1144,7 +1211,14 @@ cudaError_t launch_gemm(DeviceInfo &info, int kidx, int units, int cap, const Ma
     cluster_attr[1].val.programmaticStreamSerializationAllowed = 1;
     std::unique_lock<std::mutex> lk(g_mu);      // (calls from several host threads)
     if (!info.attr_set[kidx]) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+        // The warpgroups' register split (setmaxnreg) draws on the registers the
+        // block is launched with: a kernel built with fewer than kLaunchRegs per
+        // thread is never launched (its raise would wait forever).
+        cudaFuncAttributes fa;
+        cudaError_t e = cudaFuncGetAttributes(&fa, kern);
+        if (e != cudaSuccess) return e;
+        if (fa.numRegs < kLaunchRegs) return cudaErrorInvalidConfiguration;
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
         if (e != cudaSuccess) return e;
         int slots = info.sms;
         if (CG == 2) {
@@ -1490,8 +1564,14 @@ fp4_status gemm_impl(fp4_format fmt, int prepacked, const void *A, const void *s
     const int64_t rb_a = cdiv(rows_a, 128), rb_b = cdiv(rows_b, 128);
     const size_t atoms_a = static_cast<size_t>(rb_a * kc4 * kAtomBytes);
     const size_t atoms_b = static_cast<size_t>(rb_b * kc4 * kAtomBytes);
+    const size_t atom_bytes = prepacked ? 0 : atoms_a + atoms_b;
+    // With caller-given scratch (the static array), fewer K splits where the
+    // partials would not fit: only the atoms themselves are a hard limit.
+    if (ext_scratch)
+        while (plan.splits > 1 && atom_bytes + static_cast<size_t>(plan.splits) * rows_a * rows_b * 4 > ext_bytes)
+            --plan.splits;
     const size_t ws_bytes = plan.splits > 1 ? static_cast<size_t>(plan.splits) * rows_a * rows_b * 4 : 0;
-    size_t scratch_bytes = (prepacked ? 0 : atoms_a + atoms_b) + ws_bytes;
+    size_t scratch_bytes = atom_bytes + ws_bytes;
 
     // Split tail (direct mode): when the last wave of tiles fills at most half of
     // the resident CTA groups, each of its tiles runs as two K halves on two
@@ -1572,7 +1652,8 @@ fp4_status gemm_impl(fp4_format fmt, int prepacked, const void *A, const void *s
             a.tail_ws = reinterpret_cast<float *>(scratch + tail_off);
             a.tail_flags = reinterpret_cast<unsigned long long *>(scratch + tail_off + tail_ws_bytes);
         }
-        a.epoch = ++g_epoch;
+        a.epoch = next_epoch();
+        a.stop_after = cfg ? std::max(0, cfg->stop_after) : 0;
         a.group_b = std::max(1, std::min(a.tiles_b, 8));
         a.bf16 = out == FP4_OUT_BF16;
         a.alpha = alpha;
@@ -1582,6 +1663,7 @@ fp4_status gemm_impl(fp4_format fmt, int prepacked, const void *A, const void *s
             a.mode = kEpiRows;
             a.out = D;
             a.ldo = d_cols;
+            a.st32 = (reinterpret_cast<uintptr_t>(D) & 31u) == 0 && (d_cols * esize) % 32 == 0;
         } else if (a.splits > 1) {
             a.mode = kEpiSplitK;
             a.out = ws;
@@ -1785,13 +1867,14 @@ fp4_status grouped_impl(fp4_format fmt, int prepacked, int64_t G, const int64_t 
         a.group_b = 1;
         a.bf16 = out == FP4_OUT_BF16;
         a.mode = swap ? kEpiTransposed : kEpiRows;
+        a.st32 = (reinterpret_cast<uintptr_t>(D) & 31u) == 0 && (d_cols * esize) % 32 == 0;
         a.act = act;
         a.alpha = alpha;
         a.bias = bias;
         a.out = D;
         a.ldo = d_cols;
         a.split_units = 0;
-        a.epoch = ++g_epoch;
+        a.epoch = next_epoch();
         if (units > 0 &&
             launch_grouped(cg, bn, mx, *info, static_cast<int>(units), m, a, gp, stream) != cudaSuccess)
             result = FP4_ERR_CUDA;

@@ -22,10 +22,11 @@
 // negative part of the sum.
 //
 // Work split: a warp owns two adjacent rows of B (so a SwiGLU gate/up pair
-// stays in one warp) and walks K in passes of 1024 codes, lane l taking the 32
-// codes at 32l of each pass with one 16-byte load per row; the loads of four
-// passes of both rows are issued before any is used. The grid is sized so that
-// every warp gets the same number of row pairs.
+// stays in one warp) and walks K in units of 4096 codes, lane l taking the 128
+// codes at 128l of each unit with four 16-byte loads per row; two units live in
+// registers, so the next unit's loads are in flight while the current one is
+// computed. The grid is sized so that every warp gets the same number of row
+// pairs.
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>

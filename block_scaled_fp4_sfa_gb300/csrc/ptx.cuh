@@ -143,6 +143,14 @@ __device__ __forceinline__ void st_global_v4_hint(void *p, const uint4 &v, uint6
                  : "memory");
 }
 
+// 32 bytes (a whole sector) from one thread; the address must be 32-byte aligned.
+__device__ __forceinline__ void st_global_v8_hint(void *p, const uint32_t (&w)[8], uint64_t policy)
+{
+    asm volatile("st.global.L2::cache_hint.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8}, %9;" ::"l"(p), "r"(w[0]),
+                 "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7]), "l"(policy)
+                 : "memory");
+}
+
 __device__ __forceinline__ void st_global_b32_hint(void *p, uint32_t v, uint64_t policy)
 {
     asm volatile("st.global.L2::cache_hint.b32 [%0], %1, %2;" ::"l"(p), "r"(v), "l"(policy) : "memory");
@@ -280,6 +288,29 @@ __device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t (&r)
         : "r"(taddr));
 }
 
+// This warp's 32 lanes x 8 / 16 consecutive 32-bit TMEM columns from registers
+// (thread i writes lane i). Complete once tcgen05.wait::st returns.
+__device__ __forceinline__ void tmem_st_32x32b_x8(uint32_t taddr, const uint32_t *r)
+{
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
+                 "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_32x32b_x16(uint32_t taddr, const uint32_t *r)
+{
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
+                 "%12, %13, %14, %15, %16};" ::"r"(taddr),
+                 "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+                 "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_wait()
+{
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
 __device__ __forceinline__ void tmem_ld_wait()
 {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
@@ -295,6 +326,23 @@ __device__ __forceinline__ void tmem_ld_wait_regs(uint32_t (&r)[N])
     tmem_ld_wait();
 #pragma unroll
     for (int i = 0; i < N; ++i) asm volatile("" : "+r"(r[i]));
+}
+
+// ---- register split between warpgroups -------------------------------------------------------
+
+// Every warp of a warpgroup executes the same one; .inc waits until the CTA's
+// pool (its launch registers) has room, so the .dec's of the other warpgroups
+// must free at least what the .inc's take.
+template <uint32_t N>
+__device__ __forceinline__ void regs_raise()
+{
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
+template <uint32_t N>
+__device__ __forceinline__ void regs_lower()
+{
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
 }
 
 // ---- clusters ------------------------------------------------------------------------------
@@ -324,6 +372,18 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr)
 __device__ __forceinline__ void cluster_sync()
 {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// The same barriers for threads that reach them from different places in the
+// code (the warp-role branches): the non-.aligned forms.
+__device__ __forceinline__ void cluster_sync_any()
+{
+    asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+
+__device__ __forceinline__ void cta_sync_any()
+{
+    asm volatile("barrier.sync 0;" ::: "memory");
 }
 
 // ---- descriptors ---------------------------------------------------------------------

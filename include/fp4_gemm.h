@@ -97,13 +97,23 @@ typedef enum { FP4_FMT_NVFP4 = 0, FP4_FMT_MXFP4 = 1 } fp4_format;
  *   splits:    0 auto; else the number of K splits (swap-AB mode only).
  *   max_ctas:  0 = as many persistent CTAs as fit (one per SM); else a cap.
  *   cta_group: 0 auto; 1 = one CTA per 128-row MMA; 2 = a CTA pair (cluster
- *              of 2) per 256-row MMA (bn 128 or 256).                        */
+ *              of 2) per 256-row MMA (bn 128 or 256).
+ *   stop_after: testing the bounded waits only, 0 otherwise. n > 0: every
+ *              TMA producer of the GEMM kernel stops after filling n k-tile
+ *              stages (it loads and signals nothing for stage n or later),
+ *              so the MMA issuer's bounded wait for stage n runs out: the
+ *              launch records FP4_ERR_TIMEOUT (read it with
+ *              fp4_get_device_status), every role leaves its loop, the
+ *              kernel waits for the copies and MMAs it did issue, frees its
+ *              TMEM and returns. D is then unspecified. No MMA reads a stage
+ *              that did not land. Modes 1 and 2 only.                       */
 typedef struct {
     int32_t mode;
     int32_t bn;
     int32_t splits;
     int32_t max_ctas;
     int32_t cta_group;
+    int32_t stop_after;
 } fp4_gemm_config;
 
 /* What a call with these arguments would launch (no launch, nothing read):
@@ -250,22 +260,29 @@ fp4_status fp4_gemm_host(fp4_format fmt, const void *A, const void *sfA, const v
  * is entirely pre-reserved by another framework. The pages have no
  * counterpart; this entry point exists for such callers only.
  *
- * The reordered scales and any split-K partial sums go to one static
- * __device__ array of FP4_STATIC_SCRATCH_BYTES (16 MiB) that every device
- * loading the library holds until the process exits. Problems whose scratch
- * does not fit (2 * ceil(rows/128) * ceil(K/vec/4) * 512 bytes of atoms plus,
- * for split-K plans, splits * M * N * 4 bytes) are rejected with
- * FP4_ERR_SCRATCH_LIMIT before anything is launched. The call allocates
- * nothing and calls no allocating library routine. Nothing in the array has
- * to start at zero. Every data byte a call reads was written earlier in the
- * same call. The one exception is the split last wave's hand-off flags, which
- * count as raised only when they hold that launch's own 64-bit epoch (a value
- * no earlier call used). All calls on a device share the array, so calls
- * whose kernels overlap on the GPU (other streams, other threads) race: order
- * them on one stream.
- * The first call on a device looks up the array's device address
- * (cudaGetSymbolAddress) with that device current; make that first call
- * before any stream capture. Inputs, outputs and errors as fp4_gemm. */
+ * The reordered scales, any split-K partial sums and the split last wave's
+ * partials go to one static __device__ array of FP4_STATIC_SCRATCH_BYTES
+ * (16 MiB) that every device loading the library holds until the process
+ * exits. A plan whose split-K partials would not fit takes fewer K splits
+ * (down to none), and the split last wave is skipped when its partials do not
+ * fit; problems whose scale atoms alone do not fit (2 * ceil(rows/128) *
+ * ceil(K/vec/4) * 512 bytes) are rejected with FP4_ERR_SCRATCH_LIMIT before
+ * anything is launched. The call allocates nothing and calls no allocating
+ * library routine. Nothing in the array has to start at zero. Every data byte
+ * a call reads was written earlier in the same call. The one exception is the
+ * split last wave's hand-off flags, which count as raised only when they hold
+ * that launch's own 64-bit value: a per-process random nonce mixed with the
+ * launch count through a bijective hash, so no two launches of a process share
+ * a value and bytes left in the array by earlier calls match one with
+ * probability 2^-64 (a call recorded into a CUDA graph also zeroes its flags
+ * first, because every replay reuses the recorded value). All calls on a device
+ * share the array, so calls whose kernels overlap on the GPU (other streams,
+ * other threads) race: order them on one stream.
+ * The first call on a device loads the library's device code there (CUDA's
+ * lazy module loading), which is when the array is reserved, and looks up the
+ * array's device address (cudaGetSymbolAddress) with that device current:
+ * make that first call before the device's memory is handed to another owner,
+ * and before any stream capture. Inputs, outputs and errors as fp4_gemm. */
 fp4_status fp4_gemm_static_scratch(fp4_format fmt, const void *A, const void *sfA, const void *B,
                                    const void *sfB, float alpha, void *D, int64_t M, int64_t N,
                                    int64_t K, fp4_out_dtype out, cudaStream_t stream);

@@ -49,8 +49,10 @@ def test_library_is_sm103a_only(fp4):
 
 
 def test_status_strings(fp4):
-    for code in range(7):
-        assert fp4.status_string(code)
+    # every declared status, FP4_OK .. FP4_ERR_SCRATCH_LIMIT, has its own text
+    texts = [fp4.status_string(code) for code in range(8)]
+    assert all(texts) and len(set(texts)) == 8
+    assert "static scratch" in texts[7]
     assert fp4.status_string(99) == "unknown status"
 
 
