@@ -177,12 +177,13 @@ struct Cfg {
     static constexpr int BAR_BYTES = 512;
     static constexpr int BUDGET = kSmemLimit - 1024 - BAR_BYTES;
     static constexpr int STAGES_FIT = BUDGET / STAGE_BYTES;
-    // An even count: k-tile j uses stage j % STAGES and scale-warp group j % 2, so
-    // every use of a stage belongs to the same group (see the scale warps).
-    static constexpr int STAGES = (STAGES_FIT > 8 ? 8 : STAGES_FIT) & ~1;
+    static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
     static constexpr int SLOTS = STAGES;
     static constexpr int ACC_BUFS = BN <= 128 ? 2 : 1;
     static constexpr int SF_COLS = 4 * APK * (1 + NRB);        // TMEM columns of one k-tile's scales
+    static constexpr int SFB_COLS = 4 * APK * NRB;              // of which slot B's (after slot A's 4 * APK)
+    static constexpr int HA = APK / 2;                          // slot-A atoms staged by one scale warp
+    static constexpr int HG = APK * NRB / 2;                    // slot-B atoms staged by one scale warp
     static constexpr int SF_TMEM = ACC_BUFS * BN;               // first scale column
     static constexpr int TMEM_USED = ACC_BUFS * BN + SLOTS * SF_COLS;
     static constexpr int TMEM_COLS = TMEM_USED <= 32 ? 32 : TMEM_USED <= 64 ? 64 : TMEM_USED <= 128 ? 128
@@ -202,12 +203,12 @@ struct Cfg {
     static constexpr uint32_t SF_TX = SFA_BYTES + SFB_BYTES;        // scale bytes landing per stage (this CTA)
     static_assert(CG == 1 || CG == 2, "CTA group of 1 or 2");
     static_assert(CG == 1 || BN >= 128, "paired CTAs use N tiles of 128 or 256");
-    static_assert(STAGES >= 2 && STAGES % 2 == 0, "an even number of pipeline stages");
+    static_assert(STAGES >= 4, "at least four pipeline stages");
     static_assert(32 * STAGES + 56 <= BAR_BYTES, "barriers and flags fit");
     static_assert(TMEM_USED <= 512, "TMEM budget exceeded");
     static_assert(SMEM_BYTES <= kSmemLimit, "shared memory budget exceeded");
     static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N must be a multiple of 16 in [16, 256]");
-    static_assert(SF_COLS % 8 == 0, "scale columns go out in stores of 8 or 16");
+    static_assert(HG == 1 || HG == 2 || HG == 4, "a scale warp stores 4, 8 or 16 slot-B columns at once");
 };
 
 // Records the first error of this device (later ones are dropped).
@@ -422,6 +423,25 @@ __device__ __forceinline__ void ring_next(int &stage, uint32_t &phase)
     }
 }
 
+// How many consecutive k-tiles, from the one at (stage, phase) on, have their
+// ready barrier's phase completed (0 to 4), by one batched non-blocking test.
+// Sound because the caller has consumed every earlier phase of these barriers:
+// each barrier tested is at most one phase ahead of what the caller has seen,
+// since the look-ahead (4) does not exceed the ring (STAGES).
+template <int STAGES>
+__device__ __forceinline__ int ready_run(uint32_t bar_ready, int stage, uint32_t phase)
+{
+    static_assert(STAGES >= 4, "the look-ahead stays within one turn of the ring");
+    uint32_t b[4], p[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        b[i] = bar_ready + 8 * stage;
+        p[i] = phase;
+        ring_next<STAGES>(stage, phase);
+    }
+    return __ffs(~mbar_test4_cluster(b, p)) - 1;
+}
+
 // One epilogue pass: v holds this warp's 32 TMEM lanes x PC accumulator columns,
 // tile columns c0 .. c0 + PC - 1 (slot-B rows tg.tb * BN + c0 ...). Split tail:
 // a first half parks its fp32 partial (column-major, so a fixed column is 32
@@ -593,13 +613,14 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tmap_a, const CUten
 
     // Barriers, per stage s: full (the leader's: both CTAs' operand tiles landed),
     // full_sf (this CTA's scale atoms landed), empty (the stage's MMAs completed;
-    // the leader's commit reaches both CTAs), sf_ready (the leader's: both CTAs'
-    // scale warps have stored the stage's scales in TMEM).
+    // the leader's commit reaches both CTAs), ready (the leader's: both CTAs'
+    // scale warps have stored the stage's scales in TMEM and the leader's have
+    // seen `full`, so the MMA issuer waits on this one barrier alone).
     const uint32_t bar_full = base + C::OFF_BAR;
     const uint32_t bar_full_sf = bar_full + 8 * C::STAGES;
     const uint32_t bar_empty = bar_full_sf + 8 * C::STAGES;
-    const uint32_t bar_sf_ready = bar_empty + 8 * C::STAGES;
-    const uint32_t bar_acc_full = bar_sf_ready + 8 * C::STAGES;
+    const uint32_t bar_ready = bar_empty + 8 * C::STAGES;
+    const uint32_t bar_acc_full = bar_ready + 8 * C::STAGES;
     const uint32_t bar_acc_empty = bar_acc_full + 16;
     const uint32_t bar_drain = bar_acc_empty + 16;
     uint32_t *const tmem_holder = reinterpret_cast<uint32_t *>(base_ptr + C::OFF_BAR + 32 * C::STAGES + 40);
@@ -617,7 +638,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tmap_a, const CUten
             mbar_init(bar_full + 8 * s, 1);
             mbar_init(bar_full_sf + 8 * s, 1);
             mbar_init(bar_empty + 8 * s, 1);
-            mbar_init(bar_sf_ready + 8 * s, (kSfWarps / 2) * CG);
+            mbar_init(bar_ready + 8 * s, kSfWarps * CG);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(bar_acc_full + 8 * b, 1);
@@ -706,9 +727,11 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tmap_a, const CUten
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        // This thread issues only MMAs and commits (the scale warps stage the
-        // scales): with no tcgen05.cp of its own outstanding, its per-stage
-        // mbarrier waits cost nothing on the tensor pipe.
+        // This thread issues only MMAs and commits. The tensor pipe queues about
+        // one MMA beyond the one running, so whatever this thread does between
+        // two k-tiles' MMAs must stay short: it waits on one barrier per stage
+        // (ready), and tests up to four stages ahead in one batched, non-blocking
+        // probe, so that a run of landed stages costs one shared-memory round trip.
         if (lane == 0 && rank == 0) {
             // Instruction descriptors: MXFP4 alternates the scale byte ids 0 / 2
             // between the two K=64 halves of one 4-block atom.
@@ -720,6 +743,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tmap_a, const CUten
             const uint64_t desc_b0 = smem_desc(base + C::OFF_B, 16, 1024, 2);
             int stage = 0;
             uint32_t phase = 0;
+            int known = 0;                  // k-tiles from (stage, phase) on seen ready
             int acc = 0;
             uint32_t acc_phase = 0;
             bool ok = true;
@@ -731,12 +755,18 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tmap_a, const CUten
                 const uint32_t d_tmem = tmem + static_cast<uint32_t>(acc * BN);
                 for (int kt = kt0; kt < kt1; ++kt) {
                     // the stage's operands (both CTAs) and scales (both CTAs' TMEM) are in place
-                    if (!wait(bar_full + 8 * stage, phase, args.wait_ns, abort_flag) ||
-                        !wait_cluster(bar_sf_ready + 8 * stage, phase, args.wait_ns, abort_flag)) {
-                        ok = false;
-                        break;
+                    if (known == 0) {
+                        known = ready_run<C::STAGES>(bar_ready, stage, phase);
+                        if (known == 0) {
+                            if (!wait_cluster(bar_ready + 8 * stage, phase, args.wait_ns, abort_flag)) {
+                                ok = false;
+                                break;
+                            }
+                            known = 1;
+                        }
+                        tc_fence_after();
                     }
-                    tc_fence_after();
+                    --known;
                     const uint32_t sf = tmem + static_cast<uint32_t>(C::SF_TMEM + stage * C::SF_COLS);
                     const uint64_t da = desc_a0 + static_cast<uint64_t>((stage * C::A_BYTES) >> 4);
                     const uint64_t db = desc_b0 + static_cast<uint64_t>((stage * C::B_BYTES) >> 4);
@@ -770,76 +800,85 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tmap_a, const CUten
     } else if (warp >= kFirstSfWarp) {
         regs_lower<kLowRegs>();
         // ------------------------------------------------------------ scale warps
-        // Each TMEM lane quarter q has two scale warps, taking alternate k-tiles.
-        // For a k-tile, the warp reads its lane's line of every scale atom of the
-        // stage (16 bytes each) and stores them in this quarter's lanes of the
-        // stage's TMEM scale columns with tcgen05.st: column 4t + c of slot A holds
-        // line i, word c of atom t (the scales of row 32c + i, K-chunk t); slot B
-        // likewise per 128-row block. The MMA reads, in quarter q, column q of
-        // each slot-A group and every slot-B column, so every quarter gets the
-        // same bytes. (Copying the atoms with tcgen05.cp instead, beside the
-        // MMAs, measured 1.5-2.5x slower per k-tile on this part.)
+        // Two scale warps per TMEM lane quarter q, each staging half of every
+        // k-tile's scale atoms (half h: slot-A atoms h*HA .., slot-B atoms h*HG ..)
+        // into this quarter's lanes of the stage's TMEM scale columns with
+        // tcgen05.st, then arriving on the leader's ready barrier; in the leader,
+        // the (quarter 0, half 0) warp first waits for the stage's operand tiles
+        // (full), so that ready alone tells the MMA issuer the stage is complete.
+        // Every warp takes every k-tile, so it waits on every phase of the
+        // barriers it helps complete, in order (a parity wait is only sound when
+        // the waiter has seen the barrier's previous phase and the next one cannot
+        // complete without it), and the staging latency of a k-tile is that of
+        // half its atoms. Word c of line i of a scale atom holds the four scales
+        // of row 32c + i for one K-chunk. Slot-A atom t goes to columns
+        // 4t .. 4t+3, of which the MMA reads, in quarter q, only column 4t + q:
+        // so the warp loads just word q of its lane's line (4 bytes per atom) and
+        // stores that one column. Slot-B atom (t, rb), group g = t*NRB + rb, goes
+        // to columns 4 (APK + g) + c, all four of which the MMA reads in every
+        // quarter: the warp loads whole 16-byte lines. (Copying the atoms with
+        // tcgen05.cp instead, beside the MMAs, measured 1.5-2.5x slower per k-tile
+        // on this part; one warp per quarter staging a whole k-tile, with all four
+        // slot-A columns, left NVFP4 bound by the ring's latency at ~850 cycles
+        // per k-tile.)
         const int q = warp & 3;
-        const int grp = (warp - kFirstSfWarp) >> 2;
+        const int h = (warp - kFirstSfWarp) >> 2;
         const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
-        const uint32_t ready0 = CG == 2 ? mapa_shared(bar_sf_ready, 0) : bar_sf_ready;
+        const uint32_t ready0 = CG == 2 ? mapa_shared(bar_ready, 0) : bar_ready;
         int stage = 0;
         uint32_t phase = 0;
-        uint32_t seq = 0;
         bool ok = true;
         for (int u = pair; ok && u < args.units; u += npairs) {
             int ta, tb, split, kt0, kt1, half, tidx;
             unit_work<GROUPED>(args, u, ta, tb, split, kt0, kt1, half, tidx);
-            for (int kt = kt0; kt < kt1; ++kt, ++seq) {
-                // A group takes every other k-tile; with an even stage count those
-                // always use the group's own stages, so the group waits on every phase
-                // of exactly the barriers it helps complete, in order: a parity wait
-                // is only sound when the waiter has seen the barrier's previous phase
-                // and the next one cannot complete without it.
-                if (static_cast<int>(seq & 1u) == grp) {
-                    // this CTA's scale atoms of the stage have landed (which also means
-                    // the MMAs that read the slot's previous scales have completed)
-                    bool landed = true;
-                    if (lane == 0) landed = wait(bar_full_sf + 8 * stage, phase, args.wait_ns, abort_flag);
-                    if (!__shfl_sync(0xFFFFFFFFu, landed, 0)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    // 16 columns (four atoms) at a time: group g of four columns is
-                    // slot-A atom g (g < APK), else slot-B atom (t, rb) with
-                    // g - APK = t * NRB + rb
-                    const uint32_t col = lane_base + tmem + static_cast<uint32_t>(C::SF_TMEM + stage * C::SF_COLS);
-                    const uint8_t *sfa = base_ptr + C::OFF_SFA + stage * C::SFA_BYTES + lane * 16;
-                    const uint8_t *sfb = base_ptr + C::OFF_SFB + stage * C::SFB_BYTES + lane * 16;
+            for (int kt = kt0; kt < kt1; ++kt) {
+                // this CTA's scale atoms of the stage have landed (which also means
+                // the MMAs that read the slot's previous scales have completed)
+                bool landed = true;
+                if (lane == 0) landed = wait(bar_full_sf + 8 * stage, phase, args.wait_ns, abort_flag);
+                if (!__shfl_sync(0xFFFFFFFFu, landed, 0)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t col = lane_base + tmem + static_cast<uint32_t>(C::SF_TMEM + stage * C::SF_COLS);
+                const uint8_t *sfa = base_ptr + C::OFF_SFA + stage * C::SFA_BYTES + lane * 16 + q * 4;
+                const uint8_t *sfb = base_ptr + C::OFF_SFB + stage * C::SFB_BYTES + lane * 16;
 #pragma unroll
-                    for (int c0 = 0; c0 < C::SF_COLS; c0 += 16) {
-                        uint32_t r[16];
+                for (int i = 0; i < C::HA; ++i) {
+                    const int t = h * C::HA + i;
+                    tmem_st_32x32b_x1(col + static_cast<uint32_t>(4 * t + q),
+                                      *reinterpret_cast<const uint32_t *>(sfa + t * kAtomBytes));
+                }
+                uint32_t r[4 * C::HG];
 #pragma unroll
-                        for (int a = 0; a < 4; ++a) {
-                            const int g = c0 / 4 + a;
-                            if (4 * g < C::SF_COLS) {
-                                const uint8_t *src = g < C::APK ? sfa + g * kAtomBytes
-                                                                : sfb + (((g - C::APK) % C::NRB) * C::APK +
-                                                                         (g - C::APK) / C::NRB) * kAtomBytes;
-                                const uint4 w = *reinterpret_cast<const uint4 *>(src);
-                                r[4 * a] = w.x, r[4 * a + 1] = w.y, r[4 * a + 2] = w.z, r[4 * a + 3] = w.w;
-                            }
-                        }
-                        if (c0 + 16 <= C::SF_COLS)
-                            tmem_st_32x32b_x16(col + c0, r);
-                        else
-                            tmem_st_32x32b_x8(col + c0, r);
-                    }
-                    tmem_st_wait();
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) {
-                        if constexpr (CG == 2)
-                            mbar_arrive_cluster(ready0 + 8 * stage);
-                        else
-                            mbar_arrive(bar_sf_ready + 8 * stage);
-                    }
+                for (int i = 0; i < C::HG; ++i) {
+                    const int g = h * C::HG + i;
+                    const uint4 w =
+                        *reinterpret_cast<const uint4 *>(sfb + ((g % C::NRB) * C::APK + g / C::NRB) * kAtomBytes);
+                    r[4 * i] = w.x, r[4 * i + 1] = w.y, r[4 * i + 2] = w.z, r[4 * i + 3] = w.w;
+                }
+                const uint32_t colb = col + static_cast<uint32_t>(4 * C::APK + 4 * h * C::HG);
+                if constexpr (C::HG == 4)
+                    tmem_st_32x32b_x16(colb, r);
+                else if constexpr (C::HG == 2)
+                    tmem_st_32x32b_x8(colb, r);
+                else
+                    tmem_st_32x32b_x4(colb, r);
+                tmem_st_wait();
+                tc_fence_before();
+                bool opnd = true;
+                if (lane == 0 && rank == 0 && q == 0 && h == 0)
+                    opnd = wait(bar_full + 8 * stage, phase, args.wait_ns, abort_flag);
+                if (!__shfl_sync(0xFFFFFFFFu, opnd, 0)) {    // (also: every lane's stores are done)
+                    ok = false;
+                    break;
+                }
+                if (lane == 0) {
+                    if constexpr (CG == 2)
+                        mbar_arrive_cluster(ready0 + 8 * stage);
+                    else
+                        mbar_arrive(bar_ready + 8 * stage);
                 }
                 ring_next<C::STAGES>(stage, phase);
             }

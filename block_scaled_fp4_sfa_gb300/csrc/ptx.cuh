@@ -62,7 +62,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
 // ---- acquire / release ---------------------------------------------------------
 
 // try_wait with acquire semantics at cluster scope (for barriers that threads
-// of the peer CTA arrive on with release.cluster).
+// of the peer CTA arrive on).
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity)
 {
     uint32_t ok;
@@ -74,6 +74,29 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
         : "r"(bar), "r"(parity)
         : "memory");
     return ok != 0;
+}
+
+// Non-blocking test of four mbarrier phases at once (acquire, cluster scope):
+// bit i of the result is set when the phase of parity p[i] of barrier b[i] has
+// completed. The four tests issue back to back, so their shared-memory latency
+// is paid once.
+__device__ __forceinline__ uint32_t mbar_test4_cluster(const uint32_t (&b)[4], const uint32_t (&p)[4])
+{
+    uint32_t r0, r1, r2, r3;
+    asm volatile(
+        "{\n\t.reg .pred q0, q1, q2, q3;\n\t"
+        "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 q0, [%4], %8;\n\t"
+        "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 q1, [%5], %9;\n\t"
+        "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 q2, [%6], %10;\n\t"
+        "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 q3, [%7], %11;\n\t"
+        "selp.u32 %0, 1, 0, q0;\n\t"
+        "selp.u32 %1, 2, 0, q1;\n\t"
+        "selp.u32 %2, 4, 0, q2;\n\t"
+        "selp.u32 %3, 8, 0, q3;\n\t}"
+        : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+        : "r"(b[0]), "r"(b[1]), "r"(b[2]), "r"(b[3]), "r"(p[0]), "r"(p[1]), "r"(p[2]), "r"(p[3])
+        : "memory");
+    return r0 | r1 | r2 | r3;
 }
 
 __device__ __forceinline__ uint32_t ld_acquire_shared(uint32_t addr)
@@ -288,8 +311,20 @@ __device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t (&r)
         : "r"(taddr));
 }
 
-// This warp's 32 lanes x 8 / 16 consecutive 32-bit TMEM columns from registers
-// (thread i writes lane i). Complete once tcgen05.wait::st returns.
+// This warp's 32 lanes x 1 / 8 / 16 consecutive 32-bit TMEM columns from
+// registers (thread i writes lane i). Complete once tcgen05.wait::st returns.
+__device__ __forceinline__ void tmem_st_32x32b_x1(uint32_t taddr, uint32_t r)
+{
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(r) : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_32x32b_x4(uint32_t taddr, const uint32_t *r)
+{
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "r"(r[0]), "r"(r[1]),
+                 "r"(r[2]), "r"(r[3])
+                 : "memory");
+}
+
 __device__ __forceinline__ void tmem_st_32x32b_x8(uint32_t taddr, const uint32_t *r)
 {
     asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
@@ -362,10 +397,16 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank)
     return r;
 }
 
-// Arrive on an mbarrier given by a shared::cluster address (possibly another CTA's).
+// Arrive on an mbarrier given by a shared::cluster address (possibly another
+// CTA's), with the default release at CTA scope. The kernels use it only to hand
+// TMEM over (scale columns stored, accumulator drained), which the tcgen05 wait
+// and thread-sync fences order; no generic memory passes through it. A release
+// at cluster scope would also wait for the SM's outstanding memory traffic to be
+// acknowledged: measured, that made each such arrive cost about 1.7k cycles
+// while the operand copies were streaming.
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr)
 {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+    asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 
 // Every thread of every CTA of the cluster.
