@@ -317,16 +317,21 @@ def test_deterministic_bytes(fp4, orc):
     np.testing.assert_array_equal(c, d)
 
 
-# The last, partial wave of direct-mode one-CTA tiles runs as two K halves when it
-# fills at most half of the resident CTAs (the caps below force such tails).
+# The last, partial wave of direct-mode tiles runs as two K halves when it fills
+# at most half of the resident CTAs or CTA pairs (the caps below force such tails).
 SPLIT_TAIL_CASES = [
-    # fmt, out, M, N, K, (mode, bn, cta_group, max_ctas); one CTA per MMA (pairs do not split)
+    # fmt, out, M, N, K, (mode, bn, cta_group, max_ctas)
     ("nvfp4", "bf16", 768, 768, 1280, (1, 256, 1, 14)),     # 18 tiles on 14 CTAs: 4 split, odd k-tile count
     ("mxfp4", "f32", 768, 768, 1280, (1, 256, 1, 14)),
     ("nvfp4", "f32", 512, 1024, 1312, (1, 256, 1, 12)),     # 16 tiles on 12 CTAs: 4 split; K tail
     ("mxfp4", "bf16", 384, 640, 2048, (1, 256, 1, 6)),      # 9 tiles on 6 CTAs: 3 split; partial tiles
     ("nvfp4", "f32", 256, 256, 1024, (1, 256, 1, 0)),       # 2 tiles, every CTA free: both split
-    ("nvfp4", "bf16", 384, 640, 2048, (1, 256, 2, 10)),     # a pair: no split (control)
+    # CTA pairs (tiles of 256 x 256; each CTA of a pair parks and adds its own rows)
+    ("nvfp4", "bf16", 384, 640, 2048, (1, 256, 2, 10)),     # 6 pair tiles on 5 pairs: 1 split; partial tiles
+    ("nvfp4", "bf16", 1024, 768, 1280, (1, 256, 2, 20)),    # 12 on 10 pairs: 2 split, odd k-tile count
+    ("mxfp4", "f32", 640, 640, 2048, (1, 256, 2, 16)),      # 9 on 8 pairs: 1 split; partial tiles
+    ("nvfp4", "f32", 512, 1024, 1312, (1, 256, 2, 12)),     # 8 on 6 pairs: 2 split; K tail
+    ("mxfp4", "bf16", 512, 512, 1024, (1, 256, 2, 0)),      # 4 pair tiles, every pair free: all split
 ]
 
 
