@@ -355,6 +355,27 @@ def test_persistent_grid_cap(fp4, orc):
         check_full(orc, inp, run(fp4, inp, cfg), "cap")
 
 
+def test_repeated_calls_full_size(fp4, orc):
+    # 8192^3 NVFP4 with CTA pairs: five stages, ~14 units per pair, a split tail.
+    # Timing-dependent protocol faults (a parity wait that misses its phase shows
+    # up as a bounded wait running out) need several calls under load to show:
+    # each repeated call must end with the status clear and give the same bytes.
+    inp = W.make_config("nvfp4_8192_f32")
+    A, sfA, B, sfB = (_dev(getattr(inp, k)) for k in ("A", "sfA", "B", "sfB"))
+    D = torch.empty(inp.M, inp.N, dtype=torch.float32, device="cuda")
+    first = None
+    for _ in range(4):
+        fp4.gemm(inp.fmt, A, sfA, B, sfB, inp.alpha, D, inp.M, inp.N, inp.K, inp.out)
+        st = fp4.get_device_status()
+        assert st == fp4.FP4_OK, fp4.status_string(st)
+        got = D.cpu().numpy()
+        if first is None:
+            first = got.copy()
+        else:
+            np.testing.assert_array_equal(got, first)
+    check_sampled(orc, inp, first.astype(np.float64), n_random=4)
+
+
 # ---- the named workloads at full size, sampled -------------------------------------------
 
 SAMPLED = [n for n in W.config_names() if n != "nvfp4_128x128x256_f32"]
