@@ -225,7 +225,8 @@ def cpu_sample_rows(inp, target_s):
 
 def run_reference(args, inp):
     """The CPU oracle timed as the reference arm: each step one bounded row sample."""
-    rows = cpu_sample_rows(inp, args.ref_step_s)
+    # each step a bounded sample; the whole run stays within about two minutes
+    rows = cpu_sample_rows(inp, min(args.ref_step_s, 120.0 / max(1, args.steps + args.warmup)))
     for _ in range(args.warmup):
         oracle_rows_tflops(inp, rows[: max(1, len(rows) // 8)])
     times = []
@@ -740,7 +741,7 @@ def run_grouped(args, rank, ws, local):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--op", choices=["gemm", "fused", "grouped", "quantize"], default="gemm")
