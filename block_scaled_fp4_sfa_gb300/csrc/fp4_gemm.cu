@@ -618,6 +618,50 @@ __device__ __forceinline__ void epilogue_pass(uint32_t (&v)[PC], const Args &arg
                 }
             }
         }
+    } else if (TMA_D && args.tma_d && args.mode == kEpiTransposed && !glu) {
+        // D^T through TMA boxes: the warp's 32 GEMM columns are 32 consecutive D
+        // columns; a box is those columns x R D rows (R = 4 KB / 32 elements), laid
+        // out row by row in the staging buffer (lane l writes element l of each
+        // row, so a row's 32 writes are one contiguous piece). The TMA clips rows
+        // and columns past D; a box wholly past it is skipped.
+        const int x = tg.da + row_base;
+        const int y0 = tg.db + col0;
+        const bool cols_in = x < tg.da + tg.la;
+        auto box_done = [&](int y) {
+            fence_proxy_async_shared();
+            __syncwarp();
+            if (lane == 0 && cols_in && y < tg.db + tg.lb) {
+                tma_store_2d(tmap_d, stg, x, y, d_policy);
+                bulk_commit_group();
+            }
+        };
+        if (args.bf16) {
+#pragma unroll
+            for (int b = 0; b < PC / 64; ++b) {
+                if (lane == 0) bulk_wait_read_all();
+                __syncwarp();
+#pragma unroll
+                for (int i = 0; i < 64; ++i) {
+                    const uint16_t e = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v[64 * b + i])));
+                    asm volatile("st.shared.b16 [%0], %1;" ::"r"(stg + static_cast<uint32_t>((i * 32 + lane) * 2)),
+                                 "h"(e)
+                                 : "memory");
+                }
+                box_done(y0 + 64 * b);
+            }
+        } else {
+#pragma unroll
+            for (int b = 0; b < PC / 32; ++b) {
+                if (lane == 0) bulk_wait_read_all();
+                __syncwarp();
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                    asm volatile("st.shared.b32 [%0], %1;" ::"r"(stg + static_cast<uint32_t>((i * 32 + lane) * 4)),
+                                 "r"(v[32 * b + i])
+                                 : "memory");
+                box_done(y0 + 32 * b);
+            }
+        }
     } else if (ra < tg.la) {
         if (args.mode == kEpiSplitK) {
             // fp32 partials, transposed: for a fixed column the 32 lanes of a warp
@@ -1289,6 +1333,18 @@ bool encode_output(CUtensorMap *m, void *D, int64_t rows, int64_t cols, bool bf1
                   box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
+// The same for swap-AB's transposed tiles: a box is 32 columns x (4 KB / 32
+// elements) rows, no swizzle.
+bool encode_output_t(CUtensorMap *m, void *D, int64_t rows, int64_t cols, bool bf16)
+{
+    const int64_t esize = bf16 ? 2 : 4;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols * esize)};
+    const cuuint32_t box[2] = {32u, static_cast<cuuint32_t>(4096 / (32 * esize))};
+    return encode(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, D, dims, strides,
+                  box, CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
@@ -1797,6 +1853,11 @@ fp4_status gemm_impl(fp4_format fmt, int prepacked, const void *A, const void *s
             a.mode = kEpiTransposed;
             a.out = D;
             a.ldo = d_cols;
+            // CTA pairs store D^T with TMA boxes where the tensor map allows it
+            // (SwiGLU keeps the direct stores: its gate/up pairs meet across lanes)
+            if (plan.cg == 2 && act != FP4_ACT_SWIGLU && aligned16(D) && (d_cols * esize) % 16 == 0 &&
+                encode_output_t(&m.d, D, M, d_cols, out == FP4_OUT_BF16))
+                a.tma_d = 1;
         }
         if (launch_by_cfg(plan.cg, plan.bn, mx, *info, a.units, plan.cap, m, a, stream) != cudaSuccess) {
             result = FP4_ERR_CUDA;
@@ -1892,9 +1953,9 @@ fp4_status grouped_impl(fp4_format fmt, int prepacked, int64_t G, const int64_t 
     const bool swap = mode == 2 || (mode == 0 && (max_rows <= 256 || !rows_ok));
     if (!swap && !rows_ok) return FP4_ERR_MISALIGNED;
     // swap-AB: one CTA per 128 weight rows, a group's rows in N tiles of BN (one
-    // tile when every group fits); direct: N tiles of 256, CTA pairs for MXFP4
+    // tile when every group fits); direct: CTA pairs, N tiles of 256
     const int bn = swap ? std::max(64, pow2_bn(std::min<int64_t>(max_rows, 256))) : 256;
-    const int cg = swap ? 1 : (mx ? 2 : 1);
+    const int cg = swap ? 1 : 2;
     const int nrb = static_cast<int>(cdiv(bn, 128));
     const int64_t nb = cdiv(N, 128);                 // scale blocks of one B_g
 
