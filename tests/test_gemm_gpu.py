@@ -243,6 +243,23 @@ def test_skinny_swap_widths(fp4, orc, M):
     check_full(orc, inp, run(fp4, inp, fp4.GemmConfig(mode=2, splits=2)), "split 2")
 
 
+# Swap-AB tiles of CTA pairs leave through TMA boxes of 32 D columns x 64 (bf16)
+# or 32 (fp32) D rows: ragged D edges on both axes, both output types, N tiles of
+# 128 and 256, and D rows whose pitch is not a multiple of 16 bytes (the direct
+# stores instead).
+TRANSPOSED_CASES = [("nvfp4", "bf16", 200, 1000, 512, 256), ("nvfp4", "f32", 130, 4112, 768, 256),
+                    ("mxfp4", "bf16", 100, 600, 1024, 128), ("mxfp4", "f32", 77, 2056, 512, 128),
+                    ("nvfp4", "f32", 250, 1001, 256, 256)]
+
+
+@pytest.mark.parametrize("fmt,out,M,N,K,bn", TRANSPOSED_CASES)
+def test_swap_pairs_tma_box_edges(fp4, orc, fmt, out, M, N, K, bn):
+    inp = W.make_random(fmt, M, N, K, out=out, seed=M + N)
+    cfg = fp4.GemmConfig(mode=2, bn=bn, cta_group=2)
+    assert fp4.gemm_plan(fmt, M, N, K, out, config=cfg)["cta_group"] == 2
+    check_full(orc, inp, run(fp4, inp, cfg), "swap pair %s" % ((fmt, out, M, N, K, bn),))
+
+
 def test_k_tail_not_multiple_of_tile(fp4, orc):
     for K in (32, 96, 288, 544, 800):
         for fmt in ("nvfp4", "mxfp4"):
