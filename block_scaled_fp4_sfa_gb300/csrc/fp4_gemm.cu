@@ -8,21 +8,28 @@
 // operands, K = 64 per block-scaled MMA ("MMA Instruction K Constraint"), one
 // E4M3 scale per 16 elements ("Scale Factor Granularity") or, for MXFP4, one
 // E8M0 scale per 32 ("TMA Pipelines, Tensor Cores, and ctm-rs Interop",
-// section 1). The kernel is a persistent, warp-specialised tcgen05 GEMM:
+// section 1). The kernel is a persistent, warp-specialised tcgen05 GEMM of 640
+// threads (20 warps) per CTA, with a warpgroup register split (setmaxnreg: the
+// epilogue's two warpgroups at 168 registers, the others at 48):
 //
-//   warp 0      TMA producer (one thread): fills a ring of shared-memory
-//               stages; a stage is one k-tile (256 FP4 elements = 128 bytes
-//               per row) of both operands (128B-swizzled) and their scale atoms;
-//   warp 1      MMA issuer (one thread of the leader CTA): waits for the stage
-//               to land, copies its scale atoms into TMEM (tcgen05.cp), issues
-//               four K = 64 block-scaled MMAs into a TMEM accumulator and frees
-//               the stage;
-//   warps 2..9  epilogue: each warp drains its 32 TMEM lanes x BN/2 columns
-//               into registers, hands the accumulator back at once, then
-//               applies alpha, the bias and the activation (fp4_gemm_fused),
-//               casts and stores -- rows through a per-warp staging buffer in
-//               whole 32-byte sectors, or the transposed tile for swap-AB, or
-//               fp32 split-K partials -- while the next tile's MMAs run.
+//   warp 0       TMA producer (one thread): fills a ring of shared-memory
+//                stages; a stage is one k-tile (256 FP4 elements = 128 bytes
+//                per row) of both operands (128B-swizzled) and their scale
+//                atoms;
+//   warp 1       MMA issuer (one thread of the leader CTA): per stage waits on
+//                one `ready` barrier (batched, non-blocking look-ahead over four
+//                stages), issues four K = 64 block-scaled MMAs into a TMEM
+//                accumulator and frees the stage;
+//   warps 4..11  epilogue: each warp drains its 32 TMEM lanes x BN/2 columns
+//                into registers, hands the accumulator back at once, then
+//                applies alpha, the bias and the activation (fp4_gemm_fused),
+//                casts and stores -- in a CTA pair as TMA boxes through a 4 KB
+//                staging buffer per warp (rows, or swap-AB's transposed tiles),
+//                else with direct stores; or fp32 split-K partials -- while the
+//                next tile's MMAs run;
+//   warps 12..19 scale warps: two per TMEM lane quarter, each storing half of
+//                every k-tile's scale atoms from shared memory into the stage's
+//                TMEM scale columns (tcgen05.st), then arriving on `ready`.
 //
 // Every launch may start as a programmatic dependent of the scale reorder
 // before it; all threads wait for that grid before touching memory. The
