@@ -104,7 +104,7 @@ def peaks():
 GEMM_SOURCES = ("block_scaled_fp4_sfa_gb300/csrc/fp4_gemm.cu", "block_scaled_fp4_sfa_gb300/csrc/ptx.cuh",
                 "block_scaled_fp4_sfa_gb300/csrc/epilogue.cuh")
 GEMV_SOURCES = ("block_scaled_fp4_sfa_gb300/csrc/fp4_gemv.cu", "block_scaled_fp4_sfa_gb300/csrc/epilogue.cuh")
-QUANT_SOURCES = ("block_scaled_fp4_sfa_gb300/csrc/fp4_quant.cu",)
+QUANT_SOURCES = ("block_scaled_fp4_sfa_gb300/csrc/fp4_quant.cu", "block_scaled_fp4_sfa_gb300/csrc/ptx.cuh")
 
 
 def kernel_source_hash(sources=GEMM_SOURCES):

@@ -2092,6 +2092,12 @@ fp4_status static_scratch_address(int dev, uint8_t **out)
 }
 
 }  // namespace
+
+// Shared with the quantiser's translation unit (fp4_quant.cu): the limit of
+// its bounded waits, and its device status word (read and cleared), which
+// fp4_get_device_status reports too.
+uint64_t library_wait_limit_ns() { return wait_limit_ns(); }
+int quant_take_device_status();
 }  // namespace fp4
 
 // ============================================================================ C ABI
@@ -2318,7 +2324,8 @@ fp4_status fp4_get_device_status(cudaStream_t stream)
         const int zero = 0;
         if (cudaMemcpyToSymbol(g_status, &zero, sizeof zero) != cudaSuccess) return FP4_ERR_CUDA;
     }
-    return static_cast<fp4_status>(v);
+    const int q = fp4::quant_take_device_status();   // the quantiser's word, cleared too
+    return static_cast<fp4_status>(v != 0 ? v : q);
 }
 
 const char *fp4_status_string(fp4_status s)

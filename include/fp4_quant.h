@@ -37,8 +37,12 @@
  * another. rows == 0 or K == 0 is a no-op.
  *
  * Ownership: the caller owns every buffer; nothing is allocated.
- * Errors: argument problems return a status synchronously and launch nothing;
- * a failed launch returns FP4_ERR_CUDA. Asynchronous on `stream`, current device.
+ * Errors: argument problems return a status synchronously and launch nothing
+ * (rows above 2^31 - 1025, K above 2^31 - 1, or rows * K above 2^40:
+ * FP4_ERR_UNSUPPORTED); a failed launch returns FP4_ERR_CUDA. The kernel's
+ * waits are bounded (the limit of fp4_set_wait_limit_ms); one that runs out
+ * leaves the outputs incomplete and is reported as FP4_ERR_TIMEOUT by
+ * fp4_get_device_status. Asynchronous on `stream`, current device.
  */
 #ifndef FP4_QUANT_H
 #define FP4_QUANT_H

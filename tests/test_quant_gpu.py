@@ -88,7 +88,10 @@ def check(fp4, orc, X, fmt, layout, what=""):
     assert_same(got_s, want_s, "scales " + what)
 
 
-SHAPES = [(1, 32), (128, 64), (129, 96), (300, 1024), (257, 4128), (64, 32)]
+# rows: one partial band, whole bands, a partial second band, a chunk of two
+# bands followed by a partial one, 256-row chunks with a band wholly past the
+# matrix; K: whole and partial 4-block chunk columns in both formats
+SHAPES = [(1, 32), (128, 64), (129, 96), (300, 1024), (257, 4128), (64, 32), (384, 1056), (511, 544)]
 
 
 @pytest.mark.parametrize("fmt", ["nvfp4", "mxfp4"])
