@@ -1836,7 +1836,13 @@ fp4_status gemm_impl(fp4_format fmt, int prepacked, const void *A, const void *s
         }
         a.epoch = next_epoch();
         a.stop_after = cfg ? std::max(0, cfg->stop_after) : 0;
-        a.group_b = std::max(1, std::min(a.tiles_b, 8));
+        // Groups of 8 slot-B tiles keep the tiles in flight about square (a wave
+        // of 76 pairs spans ~9 x 8 tiles); a slot-A operand of 16 MiB or more
+        // would be read again from DRAM for every group, so it gets groups of 32
+        // (8192^3 NVFP4 fp32 220.2 -> 217.2 us, 8192 x 14336 x 4096 188.8 -> 186.6;
+        // with 8 MiB, 2048 x 28672 x 8192, 32 was slower: 173.3 -> 178.0).
+        const bool big_a = static_cast<int64_t>(rows_a) * (K / 2) >= (int64_t(16) << 20);
+        a.group_b = std::max(1, std::min(a.tiles_b, big_a ? 32 : 8));
         a.bf16 = out == FP4_OUT_BF16;
         a.alpha = alpha;
         a.act = act;
