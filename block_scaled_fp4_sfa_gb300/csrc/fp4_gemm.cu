@@ -819,12 +819,15 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap *tmap_d, const CUten
                     const uint32_t full_sf = bar_full_sf + 8 * stage;
                     if (rank == 0) mbar_arrive_expect_tx(bar_full + 8 * stage, C::OPND_TX);
                     mbar_arrive_expect_tx(full_sf, C::SF_TX);
-                    tma_load_2d<CG>(base + C::OFF_A + stage * C::A_BYTES, &tmap_a, full, kt * kBKBytes, row_a);
-                    tma_load_2d<CG>(base + C::OFF_B + stage * C::B_BYTES, &tmap_b, full, kt * kBKBytes, row_b);
+                    // the scale atoms first: they land first, and the scale warps
+                    // stage them into TMEM while the operand tiles are still landing
+                    // (measured 1-2% faster than operands first on every large shape)
                     tma_load_2d<1>(base + C::OFF_SFA + stage * C::SFA_BYTES, &tmap_sfa, full_sf,
                                    kt * C::APK * (kAtomBytes / 8), sba);
                     tma_load_2d<1>(base + C::OFF_SFB + stage * C::SFB_BYTES, &tmap_sfb, full_sf,
                                    kt * C::APK * (kAtomBytes / 8), rbb);
+                    tma_load_2d<CG>(base + C::OFF_A + stage * C::A_BYTES, &tmap_a, full, kt * kBKBytes, row_a);
+                    tma_load_2d<CG>(base + C::OFF_B + stage * C::B_BYTES, &tmap_b, full, kt * kBKBytes, row_b);
                     filled |= 1u << stage;
                     fill_parity = (fill_parity & ~(1u << stage)) | (phase << stage);
                     ring_next<C::STAGES>(stage, phase);
