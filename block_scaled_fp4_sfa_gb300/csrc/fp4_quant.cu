@@ -10,12 +10,13 @@
 //
 // The step is bound by HBM: about 2.6 bytes move per value (bf16 in, half a
 // byte of code and 1/16 or 1/32 byte of scale out). Work unit = one "chunk" of
-// 128 rows x 4 scale blocks, which is exactly one 512-byte 128x4 scale atom.
+// 256 rows x 4 scale blocks: two 128-row bands, each exactly one 512-byte 128x4
+// scale atom (one band when a row of the chunk is 512 bytes, fp32 MXFP4).
 // One persistent CTA per SM: a producer thread streams the CTA's chunks into a
 // ring of shared-memory stages with tensor-map (TMA) copies, so that the input
 // keeps flowing from HBM while sixteen consumer warps convert what has landed.
-// Every consumer warp takes 8 rows of every chunk and each of its lanes one
-// whole scale block of one row (16 or 32 values, 32 to 128 bytes), so the
+// Every consumer warp takes 8 rows of each band of every chunk and each of its
+// lanes one whole scale block of one row (16 or 32 values, 32 to 128 bytes), so the
 // block maximum, the scale and its reciprocal are worked out once per block by
 // the lane that converts it; a lane stores its block's codes in one 8- or
 // 16-byte store (a warp writes whole 32-byte sectors) and its scale byte into
@@ -65,7 +66,7 @@ constexpr int kRingBytes = 192 * 1024;              // shared memory for the sta
 constexpr int kMaxStages = 12;
 
 // The first error of a quantiser launch on this device (0 = none); read and
-// cleared by take_device_status().
+// cleared by fp4::quant_take_device_status() (part of fp4_get_device_status).
 __device__ int g_quant_status;
 
 // Four E2M1 bytes from eight values (round to nearest even, saturating at +-6,
