@@ -22,7 +22,9 @@ the slowest rank's time). `roofline` is for the GEMM kernel: its FLOPs per
 launch over its CUDA-event duration, against the dense FP4 tensor peak (the
 measured bf16 burst peak times the nominal FP4:bf16 ratio 13.5:2.25 = 6).
 `e2e` is the same metric through fp4_gemm_host with pinned host buffers, the
-host<->device copies inside the timed region. `cpu_baseline` is the fp64 CPU
+host<->device copies inside the timed region; consecutive steps alternate
+between two streams, so one step's result download overlaps the next step's
+upload (two requests in flight). `cpu_baseline` is the fp64 CPU
 oracle on a bounded row sample of the same problem, on all host cores.
 
 Multi-GPU (torchrun): replicas only -- every rank runs the same problem on its
@@ -388,36 +390,57 @@ def run_ours(args, inp, rank, ws, local, act=None, bias=None):
 
     # e2e: host buffers, pinned memory, copies inside the timed region -- through
     # fp4_gemm_host, or for a fused epilogue the same copies on the stream around
-    # fp4_gemm_fused (plain scales: it reorders them itself)
+    # fp4_gemm_fused (plain scales: it reorders them itself). Consecutive steps
+    # go to two streams in turn (each with its own result buffer, and for the
+    # fused call its own device buffers), as two requests in flight would: one
+    # step's result download overlaps the next step's upload on the full-duplex
+    # host link. The events bracket all steps on both streams.
     pA, psA, pB, psB = (t.pin_memory() for t in (hA, hsA, hB, hsB))
-    pD = torch.empty(inp.M, d_cols, dtype=odt).pin_memory()
     pbias = hbias.pin_memory() if hbias is not None else None
+    lanes = []
+    for i in range(2):
+        st = stream if i == 0 else torch.cuda.Stream()
+        lane = {"stream": st, "pD": torch.empty(inp.M, d_cols, dtype=odt).pin_memory()}
+        if fused:
+            lane.update({"A": A if i == 0 else torch.empty_like(A), "sfA": sfA if i == 0 else torch.empty_like(sfA),
+                         "B": B if i == 0 else torch.empty_like(B), "sfB": sfB if i == 0 else torch.empty_like(sfB),
+                         "D": D if i == 0 else torch.empty_like(D),
+                         "bias": dbias if (i == 0 or dbias is None) else torch.empty_like(dbias)})
+        lanes.append(lane)
 
-    def e2e_step():
+    def e2e_step(i):
+        lane = lanes[i % 2]
+        st = lane["stream"]
         if not fused:
-            fp4.gemm_host(inp.fmt, pA, psA, pB, psB, inp.alpha, pD, inp.M, inp.N, inp.K, inp.out, stream=s)
+            fp4.gemm_host(inp.fmt, pA, psA, pB, psB, inp.alpha, lane["pD"], inp.M, inp.N, inp.K, inp.out,
+                          stream=st.cuda_stream)
             return
-        for dst, src in ((A, pA), (sfA, psA), (B, pB), (sfB, psB), (dbias, pbias)):
-            if dst is not None:
-                dst.copy_(src, non_blocking=True)
-        fp4.gemm_fused(inp.fmt, A, sfA, B, sfB, inp.alpha, D, inp.M, inp.N, inp.K, inp.out, act=act, bias=dbias,
-                       stream=s)
-        pD.copy_(D, non_blocking=True)
+        with torch.cuda.stream(st):
+            for key, src in (("A", pA), ("sfA", psA), ("B", pB), ("sfB", psB), ("bias", pbias)):
+                if lane[key] is not None:
+                    lane[key].copy_(src, non_blocking=True)
+            fp4.gemm_fused(inp.fmt, lane["A"], lane["sfA"], lane["B"], lane["sfB"], inp.alpha, lane["D"], inp.M,
+                           inp.N, inp.K, inp.out, act=act, bias=lane["bias"], stream=st.cuda_stream)
+            lane["pD"].copy_(lane["D"], non_blocking=True)
 
-    e_steps = max(3, min(args.steps, 20))
-    for _ in range(2):
-        e2e_step()
+    e_steps = max(4, min(args.steps, 20))
+    for i in range(2):
+        e2e_step(i)
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(e_steps):
-        e2e_step()
+    lanes[1]["stream"].wait_event(e0)
+    for i in range(e_steps):
+        e2e_step(i)
+    done1 = torch.cuda.Event()
+    done1.record(lanes[1]["stream"])
+    stream.wait_event(done1)
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / e_steps
     h2d = sum(t.numel() * t.element_size() for t in (hA, hsA, hB, hsB) + ((hbias,) if hbias is not None else ()))
-    d2h = pD.numel() * pD.element_size()
+    d2h = lanes[0]["pD"].numel() * lanes[0]["pD"].element_size()
 
     bf16_peak, hbm_peak, peak_src = peaks()
     gemm_avg_ms = sum(gemm_ms) / len(gemm_ms)
