@@ -558,22 +558,44 @@ def run_quant(args, rank, ws, local):
            "vs_baseline": None, "dtype": in_dtype + "->e2m1", "data": "synthetic", "config": cfg}
     if args.quick:
         return res
-    # e2e: pinned host values in, codes and scales back to pinned host memory
+    # e2e: pinned host values in, codes and scales back to pinned host memory;
+    # consecutive steps on two streams in turn, each with its own buffers (as
+    # for the GEMM line: one step's download overlaps the next one's upload)
     pX = hX.pin_memory()
-    pc = torch.empty(rows * K // 2, dtype=torch.uint8).pin_memory()
-    ps = torch.empty(atom_bytes, dtype=torch.uint8).pin_memory()
-    e_steps = max(3, min(args.steps, 20))
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    lanes = []
+    for i in range(2):
+        lanes.append({"stream": stream if i == 0 else torch.cuda.Stream(),
+                      "X": Xd if i == 0 else torch.empty_like(Xd),
+                      "codes": codes if i == 0 else torch.empty_like(codes),
+                      "sf": sf if i == 0 else torch.empty_like(sf),
+                      "pc": torch.empty(rows * K // 2, dtype=torch.uint8).pin_memory(),
+                      "ps": torch.empty(atom_bytes, dtype=torch.uint8).pin_memory()})
+
+    def e2e_step(i):
+        lane = lanes[i % 2]
+        with torch.cuda.stream(lane["stream"]):
+            lane["X"].copy_(pX, non_blocking=True)
+            fp4.quantize(fmt, lane["X"], rows, K, lane["codes"], lane["sf"], in_dtype=in_dtype, layout="atom",
+                         stream=lane["stream"].cuda_stream)
+            lane["pc"].copy_(lane["codes"], non_blocking=True)
+            lane["ps"].copy_(lane["sf"], non_blocking=True)
+
+    e_steps = max(4, min(args.steps, 20))
+    for i in range(2):
+        e2e_step(i)
     torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(e_steps):
-        Xd.copy_(pX, non_blocking=True)
-        step()
-        pc.copy_(codes, non_blocking=True)
-        ps.copy_(sf, non_blocking=True)
+    lanes[1]["stream"].wait_event(e0)
+    for i in range(e_steps):
+        e2e_step(i)
+    done1 = torch.cuda.Event()
+    done1.record(lanes[1]["stream"])
+    stream.wait_event(done1)
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / e_steps
+    pc, ps = lanes[0]["pc"], lanes[0]["ps"]
     _, hbm_peak, peak_src = peaks()
     avg_ms = sum(ms) / len(ms)
     achieved = nbytes / (avg_ms * 1e-3) / 1e9
@@ -693,27 +715,43 @@ def run_grouped(args, rank, ws, local):
            "gemm_us": 1e3 * sum(gemm_ms) / len(gemm_ms)}
     if args.quick:
         return res
-    # e2e: pinned host buffers copied in, the plain-scale grouped call, D copied back
+    # e2e: pinned host buffers copied in, the plain-scale grouped call, D copied
+    # back; consecutive steps on two streams in turn, each with its own buffers
+    # (as for the GEMM line)
     pA, psA, pB, psB = (t.pin_memory() for t in (hA, hsA, hB, hsB))
-    pD = torch.empty(M, d_cols, dtype=odt).pin_memory()
+    lanes = []
+    for i in range(2):
+        lane = {"stream": stream if i == 0 else torch.cuda.Stream(),
+                "pD": torch.empty(M, d_cols, dtype=odt).pin_memory()}
+        for key, t in (("A", A), ("sfA", sfA), ("B", B), ("sfB", sfB), ("D", D)):
+            lane[key] = t if i == 0 else torch.empty_like(t)
+        lanes.append(lane)
 
-    def e2e_step():
-        for dst, src in ((A, pA), (sfA, psA), (B, pB), (sfB, psB)):
-            dst.copy_(src, non_blocking=True)
-        fp4.gemm_grouped(gin.fmt, gin.offsets, A, sfA, B, sfB, gin.alpha, D, N, K, gin.out, act=act, stream=s)
-        pD.copy_(D, non_blocking=True)
+    def e2e_step(i):
+        lane = lanes[i % 2]
+        with torch.cuda.stream(lane["stream"]):
+            for key, src in (("A", pA), ("sfA", psA), ("B", pB), ("sfB", psB)):
+                lane[key].copy_(src, non_blocking=True)
+            fp4.gemm_grouped(gin.fmt, gin.offsets, lane["A"], lane["sfA"], lane["B"], lane["sfB"], gin.alpha,
+                             lane["D"], N, K, gin.out, act=act, stream=lane["stream"].cuda_stream)
+            lane["pD"].copy_(lane["D"], non_blocking=True)
 
-    e_steps = max(3, min(args.steps, 20))
-    for _ in range(2):
-        e2e_step()
+    e_steps = max(4, min(args.steps, 20))
+    for i in range(2):
+        e2e_step(i)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(e_steps):
-        e2e_step()
+    lanes[1]["stream"].wait_event(e0)
+    for i in range(e_steps):
+        e2e_step(i)
+    done1 = torch.cuda.Event()
+    done1.record(lanes[1]["stream"])
+    stream.wait_event(done1)
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / e_steps
+    pD = lanes[0]["pD"]
     bf16_peak, hbm_peak, peak_src = peaks()
     gemm_avg_ms = sum(gemm_ms) / len(gemm_ms)
     achieved = gin.flops / (gemm_avg_ms * 1e-3) / 1e12
