@@ -1590,17 +1590,25 @@ fp4_status make_plan(int64_t M, int64_t N, int64_t K, bool rows_ok, bool mx, int
     if (splits == 0) {
         splits = 1;
         if (p.swap && tiles < slots) {
-            // Estimated cycles: waves of units x (k-tiles x per-k-tile issue time +
-            // per-unit epilogue), plus, when split, the fp32 partials written and
-            // read again and the reduce kernel's launch. Fewer splits win ties.
-            constexpr double kTileCycles = 700.0, kUnitCycles = 1500.0, kReduceCycles = 10000.0;
-            constexpr double kBytesPerCycle = 3000.0;      // HBM bytes per SM-clock cycle, whole GPU
+            // Estimated cycles: waves of units x (k-tiles x per-k-tile time + per-unit
+            // epilogue), plus, when split, the reduce launch, a set-up per split and
+            // the fp32 partials (written transposed, then read by the reduce).
+            // Fitted to a sweep of 11 skinny shapes (M 16-256, K 8192-28672):
+            // a k-tile ~700 cycles for one CTA per MMA and ~900 for a pair, the
+            // split's fixed cost ~21000 cycles, ~340 partial bytes per cycle. (An
+            // earlier model, 10000 cycles and 1500 bytes per cycle, split shapes
+            // where one split was faster: 256 x 2048 x 8192 42.6 against 23.9 us.)
+            // Fewer splits win ties.
+            const double kTileCycles = cg == 2 ? 900.0 : 700.0;
+            constexpr double kUnitCycles = 1500.0, kReduceCycles = 21000.0, kSplitCycles = 1000.0;
+            constexpr double kPartialBytesPerCycle = 340.0;
             double best = 1e30;
             for (int s = 1; s <= std::min<int64_t>(k_tiles, 16); ++s) {
                 const double waves = static_cast<double>(cdiv(tiles * s, slots));
                 double cost = waves * (static_cast<double>(cdiv(k_tiles, s)) * kTileCycles + kUnitCycles);
                 if (s > 1)
-                    cost += kReduceCycles + 2.0 * s * static_cast<double>(rows_a) * rows_b * 4.0 / kBytesPerCycle;
+                    cost += kReduceCycles + kSplitCycles * s +
+                            s * static_cast<double>(rows_a) * rows_b * 4.0 / kPartialBytesPerCycle;
                 if (cost < best - 1e-9) {
                     best = cost;
                     splits = s;

@@ -102,12 +102,15 @@ def test_static_scratch_matches_oracle_and_allocating_entry(fp4, orc, fmt, M, N,
 
 
 def test_static_scratch_takes_fewer_splits_when_partials_do_not_fit(fp4, orc):
-    # 256 x 4096 x 14336 NVFP4: the automatic swap-AB plan splits K so that its
-    # fp32 partials (splits x 4 MiB) plus the scale atoms (3.9 MiB) exceed the
-    # 16 MiB array; the call must lower the split count, not refuse the problem.
-    inp = W.make_random("nvfp4", 256, 4096, 14336, out="bf16", seed=5)
-    plan = fp4.gemm_plan("nvfp4", 256, 4096, 14336, "bf16")
-    assert plan["swap"] and plan["splits"] * 256 * 4096 * 4 + 4_000_000 > fp4.STATIC_SCRATCH_BYTES
+    # 128 x 4096 x 32768 NVFP4: the automatic swap-AB plan splits K (4 ways) so
+    # that its fp32 partials (splits x 2 MiB) plus the scale atoms (8.3 MiB)
+    # exceed the 16 MiB array; the call must lower the split count, not refuse.
+    M, N, K = 128, 4096, 32768
+    inp = W.make_random("nvfp4", M, N, K, out="bf16", seed=5)
+    plan = fp4.gemm_plan("nvfp4", M, N, K, "bf16")
+    atoms = fp4.scale_atom_bytes(M, K, 16) + fp4.scale_atom_bytes(N, K, 16)
+    assert plan["swap"] and plan["splits"] > 1
+    assert plan["splits"] * M * N * 4 + atoms > fp4.STATIC_SCRATCH_BYTES >= atoms + M * N * 4
     tensors = [_dev(getattr(inp, k)) for k in ("A", "sfA", "B", "sfB")]
     alloc = _call(fp4, "alloc", inp, tensors)
     rows = _rows(inp.M)
