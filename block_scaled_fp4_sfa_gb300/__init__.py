@@ -45,7 +45,8 @@ class Fp4Error(RuntimeError):
 class GemmConfig(ctypes.Structure):
     """fp4_gemm_config: plan overrides (0 = automatic)."""
     _fields_ = [("mode", ctypes.c_int32), ("bn", ctypes.c_int32), ("splits", ctypes.c_int32),
-                ("max_ctas", ctypes.c_int32), ("cta_group", ctypes.c_int32), ("stop_after", ctypes.c_int32)]
+                ("max_ctas", ctypes.c_int32), ("cta_group", ctypes.c_int32), ("stop_after", ctypes.c_int32),
+                ("split_tail", ctypes.c_int32)]
 
 
 class Epilogue(ctypes.Structure):

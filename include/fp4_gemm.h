@@ -37,8 +37,9 @@
  * Ownership: the caller owns every buffer; the library never frees them.
  * Calls taking plain scales reorder them into stream-ordered scratch
  * (cudaMallocAsync / cudaFreeAsync on `stream`); the partial sums of split-K
- * plans and of a split last wave (with its hand-off flags) use the same kind
- * of scratch. Nothing else is allocated per call.
+ * plans and of a split last wave (with its hand-off flags; only when
+ * fp4_gemm_config.split_tail asks for it) use the same kind of scratch.
+ * Nothing else is allocated per call.
  *
  * Errors: argument problems return a status synchronously and launch nothing.
  * Launch failures return FP4_ERR_CUDA. Every wait inside the kernels is
@@ -106,7 +107,13 @@ typedef enum { FP4_FMT_NVFP4 = 0, FP4_FMT_MXFP4 = 1 } fp4_format;
  *              fp4_get_device_status), every role leaves its loop, the
  *              kernel waits for the copies and MMAs it did issue, frees its
  *              TMEM and returns. D is then unspecified. No MMA reads a stage
- *              that did not land. Modes 1 and 2 only.                       */
+ *              that did not land. Modes 1 and 2 only.
+ *   split_tail: direct mode. 0 = automatic, which is off: on this GPU every
+ *              shape where it applied ran faster without it. 1 = when the
+ *              last, partial wave of tiles fills at most half of the resident
+ *              CTAs (or pairs), its tiles run as two K halves on two CTAs,
+ *              the second adding the first's fp32 partial in a fixed order.
+ *              Other values: FP4_ERR_INVALID_ARG.                           */
 typedef struct {
     int32_t mode;
     int32_t bn;
@@ -114,6 +121,7 @@ typedef struct {
     int32_t max_ctas;
     int32_t cta_group;
     int32_t stop_after;
+    int32_t split_tail;
 } fp4_gemm_config;
 
 /* What a call with these arguments would launch (no launch, nothing read):
@@ -260,24 +268,17 @@ fp4_status fp4_gemm_host(fp4_format fmt, const void *A, const void *sfA, const v
  * is entirely pre-reserved by another framework. The pages have no
  * counterpart; this entry point exists for such callers only.
  *
- * The reordered scales, any split-K partial sums and the split last wave's
- * partials go to one static __device__ array of FP4_STATIC_SCRATCH_BYTES
- * (16 MiB) that every device loading the library holds until the process
- * exits. A plan whose split-K partials would not fit takes fewer K splits
- * (down to none), and the split last wave is skipped when its partials do not
- * fit; problems whose scale atoms alone do not fit (2 * ceil(rows/128) *
- * ceil(K/vec/4) * 512 bytes) are rejected with FP4_ERR_SCRATCH_LIMIT before
- * anything is launched. The call allocates nothing and calls no allocating
- * library routine. Nothing in the array has to start at zero. Every data byte
- * a call reads was written earlier in the same call. The one exception is the
- * split last wave's hand-off flags, which count as raised only when they hold
- * that launch's own 64-bit value: a per-process random nonce mixed with the
- * launch count through a bijective hash, so no two launches of a process share
- * a value and bytes left in the array by earlier calls match one with
- * probability 2^-64 (a call recorded into a CUDA graph also zeroes its flags
- * first, because every replay reuses the recorded value). All calls on a device
- * share the array, so calls whose kernels overlap on the GPU (other streams,
- * other threads) race: order them on one stream.
+ * The reordered scales and any split-K partial sums go to one static
+ * __device__ array of FP4_STATIC_SCRATCH_BYTES (16 MiB) that every device
+ * loading the library holds until the process exits. The call takes the
+ * automatic plan (no split last wave). A plan whose split-K partials would not
+ * fit takes fewer K splits (down to none); problems whose scale atoms alone do
+ * not fit (2 * ceil(rows/128) * ceil(K/vec/4) * 512 bytes) are rejected with
+ * FP4_ERR_SCRATCH_LIMIT before anything is launched. The call allocates
+ * nothing and calls no allocating library routine. Nothing in the array has to
+ * start at zero: every byte a call reads was written earlier in the same call.
+ * All calls on a device share the array, so calls whose kernels overlap on the
+ * GPU (other streams, other threads) race: order them on one stream.
  * The first call on a device loads the library's device code there (CUDA's
  * lazy module loading), which is when the array is reserved, and looks up the
  * array's device address (cudaGetSymbolAddress) with that device current:

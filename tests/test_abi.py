@@ -140,6 +140,7 @@ def test_plan_host_validation_without_device(fp4):
     info.launches = 7
     assert plan(M=0) == 0 and info.launches == 0          # nothing to launch
     assert plan(cfg=ctypes.byref(fp4.GemmConfig(mode=4))) in (1, 6)   # bad mode (or no device first)
+    assert plan(cfg=ctypes.byref(fp4.GemmConfig(split_tail=2))) in (1, 6)   # split_tail is 0 or 1
 
 
 def test_grouped_host_validation_without_device(fp4):

@@ -113,10 +113,10 @@ def check_full(orc, inp, act, bias, got, what):
 
 ACTS = ["none", "relu", "relu2", "swiglu"]
 
-# fmt, out, M, N, K, config (mode, bn, cta_group, max_ctas, splits) or None
+# fmt, out, M, N, K, config (mode, bn, cta_group, max_ctas, splits[, split_tail]) or None
 PLAN_CASES = [
     ("nvfp4", "f32", 300, 520, 512, None),                       # direct, one CTA per MMA, ragged
-    ("nvfp4", "bf16", 768, 768, 1280, (1, 256, 1, 14, 0)),        # direct with the split tail
+    ("nvfp4", "bf16", 768, 768, 1280, (1, 256, 1, 14, 0, 1)),     # direct with the split tail
     ("mxfp4", "f32", 640, 384, 768, (1, 256, 2, 0, 0)),           # direct, CTA pairs
     ("mxfp4", "bf16", 520, 272, 512, (1, 128, 2, 0, 0)),          # pairs, N tile 128
     ("nvfp4", "f32", 96, 1000, 512, None),                        # swap-AB (M <= 256)
@@ -128,8 +128,9 @@ PLAN_CASES = [
 def _cfg(fp4, c):
     if c is None:
         return None
-    mode, bn, cg, cap, splits = c
-    return fp4.GemmConfig(mode=mode, bn=bn, cta_group=cg, max_ctas=cap, splits=splits)
+    mode, bn, cg, cap, splits, *tail = c
+    return fp4.GemmConfig(mode=mode, bn=bn, cta_group=cg, max_ctas=cap, splits=splits,
+                          split_tail=tail[0] if tail else 0)
 
 
 @pytest.mark.parametrize("act", ACTS)

@@ -334,8 +334,9 @@ def test_deterministic_bytes(fp4, orc):
     np.testing.assert_array_equal(c, d)
 
 
-# The last, partial wave of direct-mode tiles runs as two K halves when it fills
-# at most half of the resident CTAs or CTA pairs (the caps below force such tails).
+# Asked for (split_tail = 1), the last, partial wave of direct-mode tiles runs as
+# two K halves when it fills at most half of the resident CTAs or CTA pairs (the
+# caps below force such tails).
 SPLIT_TAIL_CASES = [
     # fmt, out, M, N, K, (mode, bn, cta_group, max_ctas)
     ("nvfp4", "bf16", 768, 768, 1280, (1, 256, 1, 14)),     # 18 tiles on 14 CTAs: 4 split, odd k-tile count
@@ -356,7 +357,7 @@ SPLIT_TAIL_CASES = [
 def test_split_tail(fp4, orc, case):
     fmt, out, M, N, K, (mode, bn, cg, cap) = case
     inp = W.make_random(fmt, M, N, K, out=out, alpha=0.5, seed=M + K)
-    cfg = fp4.GemmConfig(mode=mode, bn=bn, cta_group=cg, max_ctas=cap)
+    cfg = fp4.GemmConfig(mode=mode, bn=bn, cta_group=cg, max_ctas=cap, split_tail=1)
     a = run(fp4, inp, cfg)
     check_full(orc, inp, a, "split tail %s" % (case,))
     np.testing.assert_array_equal(a, run(fp4, inp, cfg))      # fixed summation order
@@ -373,7 +374,7 @@ def test_persistent_grid_cap(fp4, orc):
 
 
 def test_repeated_calls_full_size(fp4, orc):
-    # 8192^3 NVFP4 with CTA pairs: five stages, ~14 units per pair, a split tail.
+    # 8192^3 NVFP4 with CTA pairs: five stages, ~14 units per pair.
     # Timing-dependent protocol faults (a parity wait that misses its phase shows
     # up as a bounded wait running out) need several calls under load to show:
     # each repeated call must end with the status clear and give the same bytes.

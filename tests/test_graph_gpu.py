@@ -77,22 +77,22 @@ def replay(fp4, g):
     assert st == fp4.FP4_OK, fp4.status_string(st)
 
 
-# fmt, out, M, N, K, (mode, bn, cta_group, max_ctas, splits), act
+# fmt, out, M, N, K, (mode, bn, cta_group, max_ctas, splits, split_tail), act
 CASES = [
-    ("nvfp4", "bf16", 768, 768, 1280, (1, 256, 1, 14, 0), "none"),     # 18 tiles on 14 CTAs: 4 split
-    ("mxfp4", "f32", 512, 1024, 1312, (1, 256, 1, 12, 0), "none"),     # split last wave, K tail
-    ("nvfp4", "f32", 40, 2000, 4096, (2, 64, 1, 0, 4), "none"),        # swap-AB, split-K + reduce
-    ("mxfp4", "bf16", 384, 640, 2048, (1, 256, 2, 10, 0), "none"),     # CTA pairs
-    ("nvfp4", "f32", 1, 300, 4096, (3, 0, 0, 0, 0), "none"),           # narrow-M kernel
-    ("nvfp4", "bf16", 768, 768, 1280, (1, 256, 1, 14, 0), "swiglu"),   # fused epilogue, split last wave
+    ("nvfp4", "bf16", 768, 768, 1280, (1, 256, 1, 14, 0, 1), "none"),  # 18 tiles on 14 CTAs: 4 split
+    ("mxfp4", "f32", 512, 1024, 1312, (1, 256, 1, 12, 0, 1), "none"),  # split last wave, K tail
+    ("nvfp4", "f32", 40, 2000, 4096, (2, 64, 1, 0, 4, 0), "none"),     # swap-AB, split-K + reduce
+    ("mxfp4", "bf16", 384, 640, 2048, (1, 256, 2, 10, 0, 0), "none"),  # CTA pairs
+    ("nvfp4", "f32", 1, 300, 4096, (3, 0, 0, 0, 0, 0), "none"),        # narrow-M kernel
+    ("nvfp4", "bf16", 768, 768, 1280, (1, 256, 1, 14, 0, 1), "swiglu"),  # fused epilogue, split last wave
 ]
 
 
 @pytest.mark.parametrize("prepacked", [False, True], ids=["plain", "atoms"])
 @pytest.mark.parametrize("case", CASES, ids=lambda c: "%s_%s_%dx%dx%d_m%d_%s" % (c[:5] + (c[5][0], c[6])))
 def test_gemm_graph_replays(fp4, orc, case, prepacked):
-    fmt, out, M, N, K, (mode, bn, cg, cap, splits), act = case
-    cfg = fp4.GemmConfig(mode=mode, bn=bn, cta_group=cg, max_ctas=cap, splits=splits)
+    fmt, out, M, N, K, (mode, bn, cg, cap, splits, tail), act = case
+    cfg = fp4.GemmConfig(mode=mode, bn=bn, cta_group=cg, max_ctas=cap, splits=splits, split_tail=tail)
     inps = [W.make_random(fmt, M, N, K, out=out, alpha=0.5, b_std=0.3, seed=50 + i) for i in range(REPLAYS)]
     bias = W.make_bias(N, std=1.0, seed=7) if act != "none" else None
     bufs = {k: _dev(getattr(inps[0], k)) for k in ("A", "sfA", "B", "sfB")}

@@ -1,7 +1,6 @@
 """fp4_gemm_static_scratch: the GEMM for callers that must not allocate device
-memory. Its scratch (reordered scales, split-K partials, the split last wave's
-partials and flags) is the library's static 16 MiB device array instead of
-stream-ordered allocations.
+memory. Its scratch (reordered scales, split-K partials) is the library's
+static 16 MiB device array instead of stream-ordered allocations.
 
 Every result is checked through the C ABI twice over: element by element
 against the CPU oracle with the parity tolerances of tests/test_gemm_gpu.py
@@ -85,8 +84,8 @@ def _check(orc, inp, got, alloc, rows=None):
         assert np.all(np.abs(bf16_bits_to_f64(got[sel]) - bf16_bits_to_f64(alloc[sel])) <= bf16_ulp(alloc[sel]))
 
 
-# direct plan with reordered scales (and a split last wave); swap-AB with split-K partials;
-# the narrow-M kernel (no scratch at all)
+# direct plan with reordered scales; swap-AB with split-K partials; the narrow-M
+# kernel (no scratch at all)
 CASES = [("nvfp4", 300, 520, 1024, "f32"), ("mxfp4", 16, 1536, 2048, "bf16"), ("nvfp4", 1, 1000, 4096, "f32"),
          ("mxfp4", 640, 768, 2048, "bf16")]
 
@@ -120,8 +119,8 @@ def test_static_scratch_takes_fewer_splits_when_partials_do_not_fit(fp4, orc):
 
 
 def test_static_scratch_replayed_from_a_graph(fp4, orc):
-    # The captured call's split-tail flags sit in the shared array; replays between
-    # plain calls must each match.
+    # The captured call's reordered scales sit in the shared array, which the plain
+    # calls between the replays overwrite; every replay must match.
     inp = W.make_random("nvfp4", 300, 520, 1024, out="f32", seed=21)
     tensors = [_dev(getattr(inp, k)) for k in ("A", "sfA", "B", "sfB")]
     alloc = _call(fp4, "alloc", inp, tensors)
