@@ -363,6 +363,30 @@ def test_split_tail(fp4, orc, case):
     np.testing.assert_array_equal(a, run(fp4, inp, cfg))      # fixed summation order
 
 
+# The automatic plan on skinny and few-tile shapes, as measured fastest on GB300
+# (152 SMs) with forced plans: (M, N, K) -> (swap, N tile, CTA group, K splits).
+PLAN_CHOICES = [
+    ((16, 4096, 14336), (True, 16, 1, 4)),      # long K, few tiles: split K
+    ((64, 4096, 28672), (True, 64, 1, 4)),
+    ((16, 14336, 4096), (True, 16, 1, 1)),      # enough tiles: one pass
+    ((128, 4096, 14336), (True, 128, 2, 1)),    # a split's reduce costs more than it saves
+    ((128, 2048, 8192), (True, 128, 2, 1)),
+    ((256, 4096, 14336), (False, 128, 2, 1)),   # few pair tiles: direct, N tiles of 128
+    ((512, 2048, 8192), (False, 128, 2, 1)),
+    ((1024, 14336, 4096), (False, 256, 2, 1)),  # enough tiles: N tiles of 256
+    ((8192, 8192, 8192), (False, 256, 2, 1)),
+]
+
+
+@pytest.mark.parametrize("shape,want", PLAN_CHOICES, ids=lambda v: "x".join(map(str, v)) if len(v) == 3 else None)
+def test_automatic_plan_choices(fp4, shape, want):
+    if torch.cuda.get_device_properties(0).multi_processor_count != 152:
+        pytest.skip("the choices were measured on a 152-SM GB300")
+    M, N, K = shape
+    p = fp4.gemm_plan("nvfp4", M, N, K, "bf16", prepacked=True)
+    assert (p["swap"], p["bn"], p["cta_group"], p["splits"]) == want, p
+
+
 def test_persistent_grid_cap(fp4, orc):
     # few CTAs, many tiles each: exercises the stage / accumulator phase wrap-around
     inp = W.make_random("nvfp4", 1024, 1024, 1024, out="f32", seed=6)
